@@ -1,0 +1,479 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA chunked forward pass (one JSON line on stdout).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one forward pass over the whole workload (every (sequence, head)
+chain: gate, in-chunk cumulative sum, decayed Gram tiles, triangular inverse,
+WY factors, state read-out and update, outputs and final state).  Default
+workload: B=8, H=32, T=8192, dk=dv=128, bf16 inputs, fp32 state.
+
+Multi-GPU (torchrun, one rank per GPU): weak scaling.  Every rank owns its
+own shard of B sequences (the global batch is B * world), no data-path
+collective; the only collectives are the barrier and the max-over-ranks of
+the timed interval.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (rank 0
+only), each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from linear_attention_04_gb300.workloads import WORKLOADS, Workload, make_inputs  # noqa: E402
+
+METRIC = "KDA fwd tokens/s at B8 H32 T8K d128; % of bf16 tensor peak and HBM GB/s"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+CHUNK = 16
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def token_heads(w: Workload, inp: dict) -> int:
+    return int(sum(inp["lengths"])) * w.H
+
+
+def n_tokens(inp: dict) -> int:
+    return int(sum(inp["lengths"]))
+
+
+def algorithmic_bytes(w: Workload, inp: dict) -> int:
+    """Minimum HBM bytes of one pass: q, k, theta, v, beta read and out written
+    (e*(3dk+dv) + e + e*dv per token-head), plus the fp32 final state written
+    and the fp32 initial state read when given (4*dk*dv per chain each)."""
+    e = torch.tensor([], dtype=w.dtype).element_size()
+    per = e * (3 * w.dk + w.dv) + e + e * w.dv
+    chains = inp["N"] * w.H
+    state = 4 * w.dk * w.dv * chains
+    return token_heads(w, inp) * per + state * (2 if inp["init_state"] is not None else 1)
+
+
+def chunk_gemm_flops(w: Workload, inp: dict) -> int:
+    """6*dk*dv + 2C(3dk + 2dv) per token-head: A, P, W, U', P.U, W.S, Qt.S and
+    KhC^T.U (the triangular inverse and padding not counted)."""
+    return token_heads(w, inp) * (6 * w.dk * w.dv + 2 * CHUNK * (3 * w.dk + 2 * w.dv))
+
+
+def measured_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "linear_attention_04_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel: str, workload: str) -> tuple[int | None, str | None]:
+    """DRAM bytes per launch recorded from an ncu capture under profiles/, if
+    the kernel sources still hash to the value recorded with it."""
+    want = kernel_source_hash()
+    for f in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.txt")) +
+                    glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        kv = {}
+        with open(f) as fh:
+            for line in fh:
+                line = line.strip().lstrip("-* ")
+                if ":" in line:
+                    a, b = line.split(":", 1)
+                    kv[a.strip()] = b.strip()
+        if kv.get("traffic_kernel") == kernel and kv.get("traffic_workload") == workload:
+            if kv.get("source_hash") == want and kv.get("dram_bytes_per_launch"):
+                return int(float(kv["dram_bytes_per_launch"])), os.path.basename(f)
+    return None, None
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms in the background; keeps timestamps."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", self.gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        if not inside and self.samples:
+            # the timed region was shorter than the sampling period: nearest samples
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        smax = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(inside),
+                "power_w_max": max((num(p[3]) or 0.0) for p in inside)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def shard_sequences(n_per_rank: int, world: int, rank: int) -> range:
+    """Global sequence indices owned by `rank` under weak scaling."""
+    return range(rank * n_per_rank, (rank + 1) * n_per_rank)
+
+
+def rank_seed(base: int, rank: int) -> int:
+    return base + 1000 * rank
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample_inputs(w: Workload, n_chains: int, n_tok: int, seed: int) -> dict:
+    """A bounded sample of the workload for the CPU oracle: n_chains chains of
+    n_tok tokens each, drawn with the same recipe (on the host)."""
+    n_chains = max(1, n_chains)
+    sw = Workload(w.name + "_sample", B=n_chains, H=1, T=n_tok, dk=w.dk, dv=w.dv, dtype=w.dtype,
+                  theta=w.theta, beta=w.beta, init_std=w.init_std)
+    return make_inputs(sw, seed=seed)
+
+
+def time_oracle(inp: dict, threads: int) -> float:
+    import oracle  # CPU-baseline leg only
+
+    def f64(t):
+        return None if t is None else t.to(torch.float64).numpy()
+
+    t0 = time.perf_counter()
+    oracle.fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["theta"]), f64(inp["beta"]),
+               -5.0, f64(inp["init_state"]), nthreads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w: Workload, target_s: float, seed: int) -> dict:
+    """The oracle as it stands on the host cores, on a bounded sample sized to
+    about target_s seconds; value converted to tokens/s of the workload's H."""
+    import oracle
+    oracle.build()
+    threads = oracle.host_threads()
+    n_tok = 1024
+    probe = oracle_sample_inputs(w, threads, n_tok, seed)
+    dt = time_oracle(probe, threads)
+    rate = threads * n_tok / max(dt, 1e-6)  # token-heads/s
+    n_chains = max(threads, int(round(rate * target_s / (2 * n_tok) / threads)) * threads)
+    inp = oracle_sample_inputs(w, n_chains, 2 * n_tok, seed + 1)
+    dt = time_oracle(inp, threads)
+    th = n_chains * 2 * n_tok
+    return {"value": th / dt / w.H, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n_chains} (sequence, head) chains x {2 * n_tok} tokens of the "
+                      f"{w.name} recipe (dk={w.dk}, dv={w.dv}), fp64, {threads} threads; "
+                      f"{th} token-heads in {dt:.2f} s, converted at H={w.H} heads per token"}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    from linear_attention_04_gb300 import kda_chunk_fwd, kda_device_status, kda_select_path
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, seed=rank_seed(args.seed, rank), device=dev)
+    q, k, v, th, be = inp["q"], inp["k"], inp["v"], inp["theta"], inp["beta"]
+    init, cu = inp["init_state"], inp["cu_seqlens"]
+    path = args.path if args.path != "auto" else kda_select_path(w.dtype, w.dk, w.dv)
+    out = torch.empty((q.shape[0], q.shape[1], w.H, w.dv), dtype=w.dtype, device=dev)
+    fin = torch.empty((inp["N"], w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda_chunk_fwd(q, k, v, th, be, w.g_min, init, out, fin, cu, path=path, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = kda_device_status(clear=True)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    gpu_id = str(gpu_id) if gpu_id is not None else str(local)
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) == 36:
+        gpu_id = "GPU-" + gpu_id
+    clocks = ClockSampler(gpu_id).start()
+    time.sleep(0.3)
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    time.sleep(0.25)
+    clocks.stop()
+    total_ms = start.elapsed_time(end)
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = max_over_ranks(total_ms, world)
+    status = kda_device_status(clear=True)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed steps")
+
+    tokens = n_tokens(inp)
+    value = tokens * world * args.steps / (total_ms / 1e3)
+    ms_per_step = total_ms / args.steps
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    peaks, peak_src = measured_peaks()
+    alg = algorithmic_bytes(w, inp)
+    flops = chunk_gemm_flops(w, inp)
+    achieved = alg / avg_launch_s / 1e9
+    kname = "kda_fwd_tc_kernel" if path == "tc" else "kda_fwd_simt_kernel"
+    traffic, traffic_src = traffic_from_profiles(kname, w.name)
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": traffic, "peak_source": f"hbm_gbs of {peak_src}",
+            "kernel": kname, "algorithmic_bytes_per_launch": alg,
+            "tensor": {"achieved_tflops": round(flops / avg_launch_s / 1e12, 2),
+                       "peak_tflops": peaks["bf16_tflops"],
+                       "frac": round(flops / avg_launch_s / 1e12 / peaks["bf16_tflops"], 4),
+                       "flops_per_launch": flops}}
+    if traffic_src:
+        roof["traffic_source"] = traffic_src
+
+    # ---- end to end: pinned host buffers in, result back out, every step
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hth, hbe = (x.cpu().pin_memory() for x in (q, k, v, th, be))
+        hinit = init.cpu().pin_memory() if init is not None else None
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hfin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+        dq, dk_, dv_, dth, dbe = (torch.empty_like(x) for x in (q, k, v, th, be))
+        dinit = torch.empty_like(init) if init is not None else None
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hth, hbe)) + \
+            (hinit.numel() * 4 if hinit is not None else 0)
+        d2h = hout.numel() * hout.element_size() + hfin.numel() * 4
+
+        def e2e_step():
+            for d, h in ((dq, hq), (dk_, hk), (dv_, hv), (dth, hth), (dbe, hbe)):
+                d.copy_(h, non_blocking=True)
+            if dinit is not None:
+                dinit.copy_(hinit, non_blocking=True)
+            kda_chunk_fwd(dq, dk_, dv_, dth, dbe, w.g_min, dinit, out, fin, cu, path=path,
+                          stream=stream)
+            hout.copy_(out, non_blocking=True)
+            hfin.copy_(fin, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 10))
+        barrier(world)
+        torch.cuda.synchronize()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(s2.elapsed_time(e2), world)
+        barrier(world)
+        e2e = {"value": tokens * world * n_e2e / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "ms_per_step": round(e2e_ms / n_e2e, 3)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds, args.seed + 17)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+            if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+            "config": {"workload": f"{w.name}: B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv}, "
+                                   f"chunk 16, g_min={w.g_min}, fp32 state",
+                       "B_per_gpu": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
+                       "global_batch": w.B * world, "parallelism": f"sequence-shard x{world}",
+                       "path": path, "seed": args.seed,
+                       "l2": "inputs larger than L2 (no flush): "
+                             f"{alg / 1e9:.2f} GB per step vs 126 MB L2"},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+            "clocks": clocks.summary(t_wall0, t_wall1),
+            "kernel_ms": {"mean": round(statistics.mean(launch_ms), 4),
+                          "min": round(min(launch_ms), 4), "max": round(max(launch_ms), 4)}}
+    return line
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    import oracle
+    w = WORKLOADS[args.workload]
+    oracle.build()
+    threads = oracle.host_threads()
+    # size one step's sample to about args.ref_step_seconds of oracle work
+    n_tok = 1024
+    probe = oracle_sample_inputs(w, threads, n_tok, args.seed)
+    dt = time_oracle(probe, threads)
+    rate = threads * n_tok / max(dt, 1e-6)
+    n_chains = max(threads, int(round(rate * args.ref_step_seconds / n_tok / threads)) * threads)
+    inp = oracle_sample_inputs(w, n_chains, n_tok, args.seed + 1)
+    for _ in range(args.warmup):
+        time_oracle(inp, threads)
+    times = [time_oracle(inp, threads) for _ in range(args.steps)]
+    th = n_chains * n_tok
+    total = sum(times)
+    value = th * args.steps / total / w.H
+    sample = (f"{n_chains} (sequence, head) chains x {n_tok} tokens of the {w.name} recipe per "
+              f"step, fp64 oracle, {threads} threads, converted at H={w.H} heads per token")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name}: B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv}, "
+                                   f"chunk 16, g_min={w.g_min} (bounded sample per step)",
+                       "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="train_bf16")
+    ap.add_argument("--path", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--seed", type=int, default=20261204)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: at least 3 warm-up steps are required; using 3", file=sys.stderr)
+        args.warmup = 3
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            if rank != 0:
+                return 0
+            line = run_reference(args, rank, world)
+        else:
+            line = run_ours(args, rank, world, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            if dist.is_initialized():
+                dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,152 @@
+/*
+ * kda.h -- C ABI of libkda.so: the chunk-parallel forward pass of Kimi Delta
+ * Attention (KDA) on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (per sequence s and head h, tokens t of that sequence):
+ *
+ *   g_t = g_min * sigmoid(theta_t)                               (dk vector)
+ *   S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *   o_t = S_t^T q_t
+ *
+ * The bounded gate is eq. 1 of "Architecture Deep Dive: Kimi K3's MoE, Linear
+ * Attention, and Long-Context Engineering" (sec. 3.2, gamma_min = -5) and the
+ * scaled-sigmoid log-decay of "Kimi K3 Deep Dive" (section "The Design").  The
+ * recurrence is the gated delta rule with channel-wise forgetting that the
+ * "Kimi K3" explainer (section "Across the sequence") describes: a fixed-size
+ * state S in R^{dk x dv} that each token reads, selectively forgets and writes.
+ * The library evaluates it chunk by chunk (16-token chunks, "Kimi K3 Deep
+ * Dive", section "The Problem"), every tile through dense products.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers are DEVICE pointers on the current CUDA device.  The caller owns
+ * every buffer; the library allocates nothing per call.  Inputs are read
+ * only; out and final_state are overwritten.  All calls are asynchronous on
+ * `stream` and return as soon as the work is queued.
+ *
+ * Layouts (row-major, contiguous):
+ *   fixed length (cu_seqlens == NULL):
+ *     q, k, theta  [B, T, H, dk]      v, out  [B, T, H, dv]      beta [B, T, H]
+ *     init_state, final_state  fp32 [B, H, dk, dv]   (row i = key channel)
+ *   packed variable length (cu_seqlens != NULL):
+ *     B is the number of sequences and T the total number of tokens; the
+ *     tensors are [1, T, H, .]; cu_seqlens is int32 [B + 1] on the device with
+ *     cu_seqlens[0] = 0, cu_seqlens[B] = T, non-decreasing; sequence s is the
+ *     tokens [cu_seqlens[s], cu_seqlens[s+1]).  States are [B, H, dk, dv].
+ *     The state restarts from init_state[s] (or zero) at every sequence start.
+ *   init_state == NULL: every sequence starts from the zero state.
+ *   final_state == NULL: the final state is not written.
+ *   Lengths need not be multiples of 16: the last chunk of a sequence is
+ *   masked (exactly as if padded with k = v = beta = 0, theta = -inf).
+ *
+ * Semantics: no scaling of q and no normalisation of q or k is applied (the
+ * caller normalises); beta is used as given (already in (0, 1)); g_min must be
+ * negative.  o_t is read after the token-t update.
+ *
+ * Shapes: dk, dv in {16, 32, 64, 128}; B, H >= 1; T >= 0.
+ * Alignment: every tensor pointer 16-byte aligned.
+ *
+ * Errors: every entry point returns KDA_OK (0) or a negative KDA_ERR_* code
+ * and never throws.  Argument errors are found on the host before anything
+ * is queued.  A device-side wait that runs out (the tensor-core path bounds
+ * every wait) records KDA_ERR_DEVICE_TIMEOUT in a per-device status word that
+ * kda_device_status() reads after the caller has synchronised.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+/* status codes */
+#define KDA_OK 0
+#define KDA_ERR_INVALID_ARG (-1)        /* null pointer, bad size, bad g_min, bad enum   */
+#define KDA_ERR_MISALIGNED (-2)         /* a tensor pointer not 16-byte aligned          */
+#define KDA_ERR_UNSUPPORTED_DEVICE (-3) /* current device is not compute capability 10.3 */
+#define KDA_ERR_LAUNCH (-4)             /* the CUDA launch itself failed                 */
+#define KDA_ERR_DEVICE_TIMEOUT (-5)     /* a bounded device wait ran out (status word)   */
+#define KDA_ERR_CUDA (-6)               /* another CUDA runtime error                    */
+#define KDA_ERR_UNSUPPORTED_SHAPE (-7)  /* dk/dv outside {16,32,64,128} for this path    */
+
+/* kernel path selection for kda_chunk_fwd_ex */
+#define KDA_PATH_AUTO 0 /* tensor-core path for bf16 when available, else SIMT        */
+#define KDA_PATH_SIMT 1 /* fp32 CUDA-core path (any supported dtype/shape)             */
+#define KDA_PATH_TC 2   /* tcgen05/TMEM tensor-core path (bf16, dk = dv = 128)         */
+
+/* element types of q, k, v, theta, beta and out */
+#define KDA_DTYPE_BF16 0
+#define KDA_DTYPE_F32 1
+
+/*
+ * kda_chunk_fwd -- bf16 q, k, v, theta, beta and out; fp32 states; fp32
+ * arithmetic in the gate and the state, bf16 tensor-core operands.
+ * Arguments as in the header comment above.  Returns KDA_OK or KDA_ERR_*.
+ */
+KDA_API int kda_chunk_fwd(const void* q, const void* k, const void* v, const void* theta,
+                          const void* beta, float g_min, const float* init_state, void* out,
+                          float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
+                          int dk, int dv, cudaStream_t stream);
+
+/*
+ * kda_chunk_fwd_f32 -- identical argument list with fp32 q, k, v, theta, beta
+ * and out.  Computed entirely in fp32 on CUDA cores (no reduced-precision
+ * operands), for callers that need fp32 accuracy.
+ */
+KDA_API int kda_chunk_fwd_f32(const float* q, const float* k, const float* v, const float* theta,
+                              const float* beta, float g_min, const float* init_state, float* out,
+                              float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
+                              int dk, int dv, cudaStream_t stream);
+
+/* Extended call: the same operation with the dtype and the kernel path chosen
+ * explicitly.  `dtype` is KDA_DTYPE_*; `path` is KDA_PATH_*.  KDA_PATH_TC
+ * requires dtype bf16 and dk = dv = 128 (else KDA_ERR_UNSUPPORTED_SHAPE). */
+typedef struct kda_fwd_args {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* theta;
+  const void* beta;
+  float g_min;
+  const float* init_state;
+  void* out;
+  float* final_state;
+  const int32_t* cu_seqlens;
+  int B, H, T, dk, dv;
+  int dtype;
+  int path;
+} kda_fwd_args;
+
+KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* args, cudaStream_t stream);
+
+/* Reads the current device's status word (KDA_OK or KDA_ERR_DEVICE_TIMEOUT).
+ * Synchronous with respect to the device's prior work only through the copy:
+ * call after synchronising the streams that ran the forward pass.  A nonzero
+ * `clear` resets the word to KDA_OK. */
+KDA_API int kda_device_status(int clear);
+
+/* The kernel path kda_chunk_fwd_ex would take for these arguments with
+ * KDA_PATH_AUTO (KDA_PATH_TC or KDA_PATH_SIMT), or a negative KDA_ERR_*. */
+KDA_API int kda_select_path(int dtype, int dk, int dv);
+
+/* Human-readable text for a status code (static storage, never NULL). */
+KDA_API const char* kda_strerror(int code);
+
+/* Library version as 10000*major + 100*minor + patch. */
+KDA_API int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,172 @@
+// kda_api.cu -- the C ABI of libkda.so: argument checks, path choice, launch.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "kda.h"
+#include "kda_internal.cuh"
+
+namespace kda {
+
+// Per-device status word: kernels that give up on a bounded wait store
+// KDA_ERR_DEVICE_TIMEOUT here.  Static device memory, one word per device.
+__device__ int g_status_word = 0;
+
+int* status_word_device_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_dev_once[kMaxDevices];
+int g_dev_ok[kMaxDevices];  // 1 = compute capability 10.3, 0 = other, -1 = query failed
+
+int check_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return KDA_ERR_CUDA;
+  if (dev >= kMaxDevices) return KDA_ERR_UNSUPPORTED_DEVICE;
+  std::call_once(g_dev_once[dev], [dev]() {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      g_dev_ok[dev] = -1;
+      return;
+    }
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : 0;
+  });
+  if (g_dev_ok[dev] < 0) return KDA_ERR_CUDA;
+  return g_dev_ok[dev] ? KDA_OK : KDA_ERR_UNSUPPORTED_DEVICE;
+}
+
+bool shape_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate(const kda_fwd_args* a) {
+  if (!a) return KDA_ERR_INVALID_ARG;
+  if (a->B <= 0 || a->H <= 0 || a->T < 0) return KDA_ERR_INVALID_ARG;
+  // token tensors may be empty (null) only when there are no tokens
+  if (a->T > 0 && (!a->q || !a->k || !a->v || !a->theta || !a->beta || !a->out))
+    return KDA_ERR_INVALID_ARG;
+  if (!(a->g_min < 0.0f) || a->g_min != a->g_min) return KDA_ERR_INVALID_ARG;
+  if (a->dtype != KDA_DTYPE_BF16 && a->dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+  if (a->path != KDA_PATH_AUTO && a->path != KDA_PATH_SIMT && a->path != KDA_PATH_TC)
+    return KDA_ERR_INVALID_ARG;
+  if (!shape_ok(a->dk) || !shape_ok(a->dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
+  // sizes must fit the 32-bit grid and 64-bit offsets used by the kernels
+  const int64_t chains = (int64_t)a->B * a->H;
+  if (chains > (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
+  if (!a->cu_seqlens && (int64_t)a->B * a->T > ((int64_t)1 << 40)) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {a->q, a->k, a->v, a->theta, a->beta, a->out, a->init_state,
+                        a->final_state, a->cu_seqlens};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_MISALIGNED;
+  return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
+extern "C" {
+
+KDA_API int kda_select_path(int dtype, int dk, int dv) {
+  if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+  if (!kda::shape_ok(dk) || !kda::shape_ok(dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
+  return kda::tc_supported(dtype, dk, dv) ? KDA_PATH_TC : KDA_PATH_SIMT;
+}
+
+KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* a, cudaStream_t stream) {
+  int rc = kda::validate(a);
+  if (rc != KDA_OK) return rc;
+  int path = a->path;
+  if (path == KDA_PATH_AUTO) path = kda_select_path(a->dtype, a->dk, a->dv);
+  if (path == KDA_PATH_TC && !kda::tc_supported(a->dtype, a->dk, a->dv))
+    return KDA_ERR_UNSUPPORTED_SHAPE;
+  rc = kda::check_device();
+  if (rc != KDA_OK) return rc;
+  const bool empty = a->T == 0;
+  kda::FwdParams p;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.theta = a->theta;
+  p.beta = a->beta;
+  p.g_min = a->g_min;
+  p.init_state = a->init_state;
+  p.out = a->out;
+  p.final_state = a->final_state;
+  p.cu_seqlens = a->cu_seqlens;
+  p.N = a->B;
+  p.H = a->H;
+  p.T = a->T;
+  p.dk = a->dk;
+  p.dv = a->dv;
+  p.dtype = a->dtype;
+  if (empty && !a->cu_seqlens) {
+    // no tokens: the final state is the initial state
+    if (a->final_state) {
+      size_t bytes = (size_t)a->B * a->H * a->dk * a->dv * sizeof(float);
+      cudaError_t e = a->init_state
+                          ? cudaMemcpyAsync(a->final_state, a->init_state, bytes,
+                                            cudaMemcpyDeviceToDevice, stream)
+                          : cudaMemsetAsync(a->final_state, 0, bytes, stream);
+      if (e != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+  }
+  if (path == KDA_PATH_TC) return kda::launch_tc(p, stream);
+  return kda::launch_simt(p, stream);
+}
+
+KDA_API int kda_chunk_fwd(const void* q, const void* k, const void* v, const void* theta,
+                          const void* beta, float g_min, const float* init_state, void* out,
+                          float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
+                          int dk, int dv, cudaStream_t stream) {
+  kda_fwd_args a{q, k, v, theta, beta, g_min, init_state, out, final_state, cu_seqlens,
+                 B, H, T, dk, dv, KDA_DTYPE_BF16, KDA_PATH_AUTO};
+  return kda_chunk_fwd_ex(&a, stream);
+}
+
+KDA_API int kda_chunk_fwd_f32(const float* q, const float* k, const float* v, const float* theta,
+                              const float* beta, float g_min, const float* init_state, float* out,
+                              float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
+                              int dk, int dv, cudaStream_t stream) {
+  kda_fwd_args a{q, k, v, theta, beta, g_min, init_state, out, final_state, cu_seqlens,
+                 B, H, T, dk, dv, KDA_DTYPE_F32, KDA_PATH_SIMT};
+  return kda_chunk_fwd_ex(&a, stream);
+}
+
+KDA_API int kda_device_status(int clear) {
+  int* p = kda::status_word_device_ptr();
+  if (!p) return KDA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KDA_ERR_CUDA;
+  if (clear) {
+    int z = 0;
+    if (cudaMemcpy(p, &z, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return KDA_ERR_CUDA;
+  }
+  return v;
+}
+
+KDA_API const char* kda_strerror(int code) {
+  switch (code) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+    case KDA_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3";
+    case KDA_ERR_LAUNCH: return "kernel launch failed";
+    case KDA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+    case KDA_ERR_CUDA: return "CUDA runtime error";
+    case KDA_ERR_UNSUPPORTED_SHAPE: return "unsupported (dtype, dk, dv) for this kernel path";
+    default: return "unknown status code";
+  }
+}
+
+KDA_API int kda_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,46 @@
+// Internal declarations shared by the translation units of libkda.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Chunk length of the chunk-parallel form ("Kimi K3 Deep Dive", section "The
+// Problem": a 16-token chunk matches the tensor-core GEMM granularity).
+constexpr int kChunk = 16;
+
+// Validated launch parameters shared by the kernel paths.
+struct FwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* theta;
+  const void* beta;
+  float g_min;
+  const float* init_state;
+  void* out;
+  float* final_state;
+  const int32_t* cu_seqlens;  // device, or nullptr for fixed length
+  int N;                      // sequences (B for fixed length)
+  int H, T, dk, dv;
+  int dtype;                  // KDA_DTYPE_*
+};
+
+// Device status word of the current device (bounded waits write it).
+int* status_word_device_ptr();
+
+int launch_simt(const FwdParams& p, cudaStream_t stream);
+int launch_tc(const FwdParams& p, cudaStream_t stream);
+bool tc_supported(int dtype, int dk, int dv);
+
+// Rank-ordered chain lookup for packed variable-length batches: blockIdx.x = r * H + h
+// runs the r-th longest sequence first (longest-processing-time order).  For
+// fixed-length batches the order is the natural one.  Small enough to inline
+// in each kernel; all threads of the block must call it.
+constexpr int kMaxRankedSeqs = 4096;
+
+}  // namespace kda

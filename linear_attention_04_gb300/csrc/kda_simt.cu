@@ -1,0 +1,256 @@
+// kda_simt.cu -- fp32 CUDA-core path of the KDA chunked forward pass.
+//
+// One CTA per (sequence, head, dv-slice of DVS columns).  The state slice
+// S[dk][DVS] lives in shared memory in fp32; every product is an fp32 FMA.
+// This path serves fp32 inputs (where bf16 tensor-core operands would not
+// meet fp32 accuracy) and any (dk, dv) in {16, 32, 64, 128}; for bf16 inputs
+// it is the reference-accuracy GPU path the tensor-core kernel is tested
+// beside.
+//
+// Per 16-token chunk, with the inclusive in-chunk cumulative log-decay G
+// (the decay product Gamma_ij of "Kimi K3 Deep Dive", section "The Problem",
+// is exp(G_j - G_i); with g >= g_min = -5 every factor below is at most
+// e^{80}, "Architecture Deep Dive", sec. 3.2):
+//   Kt = K e^{G}, Kh = K e^{-G}, Qt = Q e^{G}, KhC = K e^{G_C - G}
+//   A = strict_lower(Diag(beta) Kt Kh^T),  P = lower_incl_diag(Qt Kh^T)
+//   Tm = (I + A)^{-1}  (forward substitution, one thread per column)
+//   W = Tm Diag(beta) Kt,  U' = Tm Diag(beta) V
+//   U = U' - W S,  O = Qt S + P U,  S <- Diag(e^{G_C}) S + KhC^T U
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda_device.cuh"
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kSimtThreads = 128;
+constexpr int C = kChunk;
+
+template <int DK, int DVS>
+struct SimtSmem {
+  float Kt[C][DK];   // Kt, overwritten in place by W
+  float Kh[C][DK];
+  float Qt[C][DK];
+  float KhC[C][DK];
+  float eGC[DK];     // e^{G_C}
+  float S[DK][DVS];
+  float V[C][DVS];   // V, then U' and U
+  float A[C][C + 1];
+  float P[C][C + 1];
+  float Tm[C][C + 1];
+  float beta[C];
+  int rank_scratch[kMaxRankedSeqsDev + 1];
+};
+
+template <typename Tin, int DK, int DVS>
+__global__ void __launch_bounds__(kSimtThreads)
+    kda_fwd_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+                        const Tin* __restrict__ v, const Tin* __restrict__ theta,
+                        const Tin* __restrict__ beta, float g_min,
+                        const float* __restrict__ init_state, Tin* __restrict__ out,
+                        float* __restrict__ final_state, const int32_t* __restrict__ cu_seqlens,
+                        int N, int H, int T, int dv) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SimtSmem<DK, DVS>& sm = *reinterpret_cast<SimtSmem<DK, DVS>*>(smem_raw);
+  const int tid = threadIdx.x;
+  const Chain ch = chain_for_block(blockIdx.x, H, N, T, cu_seqlens, sm.rank_scratch);
+  const int h = ch.head;
+  const int j0 = blockIdx.y * DVS;  // first value column of this slice
+  const int64_t state_off = ((int64_t)ch.seq * H + h) * DK * dv;
+
+  // initial state slice
+  for (int e = tid; e < DK * DVS; e += kSimtThreads) {
+    int i = e / DVS, j = e % DVS;
+    sm.S[i][j] = init_state ? init_state[state_off + (int64_t)i * dv + j0 + j] : 0.0f;
+  }
+  __syncthreads();
+
+  for (int64_t c0 = ch.t0; c0 < ch.t1; c0 += C) {
+    const int n = (int)min((int64_t)C, ch.t1 - c0);  // valid rows of this chunk
+
+    // --- gate + in-chunk cumulative sum, decayed operands (one column per thread)
+    for (int col = tid; col < DK; col += kSimtThreads) {
+      float G = 0.0f;
+      float Gr[C];
+      float kr[C], qr[C];
+#pragma unroll
+      for (int r = 0; r < C; ++r) {
+        if (r < n) {
+          const int64_t row = (c0 + r) * H + h;
+          float th = to_f32(theta[row * DK + col]);
+          float g = g_min * (1.0f / (1.0f + expf(-th)));
+          G += g;
+          kr[r] = to_f32(k[row * DK + col]);
+          qr[r] = to_f32(q[row * DK + col]);
+        } else {
+          kr[r] = 0.0f;
+          qr[r] = 0.0f;
+        }
+        Gr[r] = G;
+      }
+      const float GC = G;
+#pragma unroll
+      for (int r = 0; r < C; ++r) {
+        float eg = expf(Gr[r]);
+        float emg = expf(-Gr[r]);
+        sm.Kt[r][col] = kr[r] * eg;
+        sm.Kh[r][col] = kr[r] * emg;
+        sm.Qt[r][col] = qr[r] * eg;
+        sm.KhC[r][col] = kr[r] * expf(GC - Gr[r]);
+      }
+      sm.eGC[col] = expf(GC);
+    }
+    for (int e = tid; e < C * DVS; e += kSimtThreads) {
+      int r = e / DVS, j = e % DVS;
+      sm.V[r][j] = (r < n) ? to_f32(v[((c0 + r) * H + h) * (int64_t)dv + j0 + j]) : 0.0f;
+    }
+    if (tid < C) sm.beta[tid] = (tid < n) ? to_f32(beta[(c0 + tid) * H + h]) : 0.0f;
+    __syncthreads();
+
+    // --- A = strict_lower(Diag(beta) Kt Kh^T), P = lower_incl_diag(Qt Kh^T)
+    for (int e = tid; e < C * C; e += kSimtThreads) {
+      int r = e / C, s = e % C;
+      float a = 0.0f, p = 0.0f;
+      if (s <= r) {
+        for (int col = 0; col < DK; ++col) {
+          float kh = sm.Kh[s][col];
+          a += sm.Kt[r][col] * kh;
+          p += sm.Qt[r][col] * kh;
+        }
+      }
+      sm.A[r][s] = (s < r) ? sm.beta[r] * a : 0.0f;
+      sm.P[r][s] = p;
+    }
+    __syncthreads();
+
+    // --- Tm = (I + A)^{-1}: column j by forward substitution
+    if (tid < C) {
+      const int j = tid;
+      float tcol[C];
+#pragma unroll
+      for (int i = 0; i < C; ++i) tcol[i] = 0.0f;
+      tcol[j] = 1.0f;
+#pragma unroll
+      for (int i = 0; i < C; ++i) {
+        if (i > j) {
+          float acc = 0.0f;
+          for (int l = j; l < i; ++l) acc += sm.A[i][l] * tcol[l];
+          tcol[i] = -acc;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < C; ++i) sm.Tm[i][j] = tcol[i];
+    }
+    __syncthreads();
+
+    // --- W = Tm Diag(beta) Kt (in place over Kt); U' = Tm Diag(beta) V (in place over V)
+    for (int col = tid; col < DK; col += kSimtThreads) {
+      float kb[C];
+#pragma unroll
+      for (int s = 0; s < C; ++s) kb[s] = sm.beta[s] * sm.Kt[s][col];
+#pragma unroll
+      for (int r = 0; r < C; ++r) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int s = 0; s < C; ++s) acc += sm.Tm[r][s] * kb[s];
+        sm.Kt[r][col] = acc;
+      }
+    }
+    for (int j = tid; j < DVS; j += kSimtThreads) {
+      float vb[C];
+#pragma unroll
+      for (int s = 0; s < C; ++s) vb[s] = sm.beta[s] * sm.V[s][j];
+#pragma unroll
+      for (int r = 0; r < C; ++r) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int s = 0; s < C; ++s) acc += sm.Tm[r][s] * vb[s];
+        sm.V[r][j] = acc;
+      }
+    }
+    __syncthreads();
+
+    // --- U = U' - W S
+    for (int e = tid; e < C * DVS; e += kSimtThreads) {
+      int r = e / DVS, j = e % DVS;
+      float acc = 0.0f;
+      for (int col = 0; col < DK; ++col) acc += sm.Kt[r][col] * sm.S[col][j];
+      sm.V[r][j] -= acc;
+    }
+    __syncthreads();
+
+    // --- O = Qt S + P U
+    for (int e = tid; e < C * DVS; e += kSimtThreads) {
+      int r = e / DVS, j = e % DVS;
+      if (r < n) {
+        float acc = 0.0f;
+        for (int col = 0; col < DK; ++col) acc += sm.Qt[r][col] * sm.S[col][j];
+        for (int s = 0; s <= r; ++s) acc += sm.P[r][s] * sm.V[s][j];
+        out[((c0 + r) * H + h) * (int64_t)dv + j0 + j] = from_f32<Tin>(acc);
+      }
+    }
+    __syncthreads();
+
+    // --- S <- Diag(e^{G_C}) S + KhC^T U
+    for (int e = tid; e < DK * DVS; e += kSimtThreads) {
+      int i = e / DVS, j = e % DVS;
+      float acc = sm.eGC[i] * sm.S[i][j];
+#pragma unroll
+      for (int r = 0; r < C; ++r) acc += sm.KhC[r][i] * sm.V[r][j];
+      sm.S[i][j] = acc;
+    }
+    __syncthreads();
+  }
+
+  if (final_state) {
+    for (int e = tid; e < DK * DVS; e += kSimtThreads) {
+      int i = e / DVS, j = e % DVS;
+      final_state[state_off + (int64_t)i * dv + j0 + j] = sm.S[i][j];
+    }
+  }
+}
+
+template <typename Tin, int DK, int DVS>
+int launch_simt_t(const FwdParams& p, cudaStream_t stream) {
+  auto kern = kda_fwd_simt_kernel<Tin, DK, DVS>;
+  const size_t smem = sizeof(SimtSmem<DK, DVS>);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return KDA_ERR_LAUNCH;
+  dim3 grid((unsigned)(p.N * p.H), (unsigned)(p.dv / DVS));
+  kern<<<grid, kSimtThreads, smem, stream>>>(
+      (const Tin*)p.q, (const Tin*)p.k, (const Tin*)p.v, (const Tin*)p.theta, (const Tin*)p.beta,
+      p.g_min, p.init_state, (Tin*)p.out, p.final_state, p.cu_seqlens, p.N, p.H, p.T, p.dv);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+template <typename Tin, int DK>
+int launch_simt_dk(const FwdParams& p, cudaStream_t stream) {
+  switch (p.dv) {
+    case 16: return launch_simt_t<Tin, DK, 16>(p, stream);
+    default: return launch_simt_t<Tin, DK, 32>(p, stream);  // dv in {32, 64, 128}
+  }
+}
+
+template <typename Tin>
+int launch_simt_dtype(const FwdParams& p, cudaStream_t stream) {
+  switch (p.dk) {
+    case 16: return launch_simt_dk<Tin, 16>(p, stream);
+    case 32: return launch_simt_dk<Tin, 32>(p, stream);
+    case 64: return launch_simt_dk<Tin, 64>(p, stream);
+    case 128: return launch_simt_dk<Tin, 128>(p, stream);
+    default: return KDA_ERR_UNSUPPORTED_SHAPE;
+  }
+}
+
+}  // namespace
+
+int launch_simt(const FwdParams& p, cudaStream_t stream) {
+  if (p.dtype == KDA_DTYPE_F32) return launch_simt_dtype<float>(p, stream);
+  return launch_simt_dtype<__nv_bfloat16>(p, stream);
+}
+
+}  // namespace kda

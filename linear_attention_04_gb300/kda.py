@@ -1,0 +1,166 @@
+"""Thin Python binding of libkda.so (argument marshalling only).
+
+Every step of the forward pass runs in the library's CUDA kernels; this module
+only checks tensor metadata, allocates outputs with torch when the caller did
+not pass them, and forwards raw device pointers and sizes through ctypes.
+There is no fallback: if the library cannot be loaded the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = -1
+KDA_ERR_MISALIGNED = -2
+KDA_ERR_UNSUPPORTED_DEVICE = -3
+KDA_ERR_LAUNCH = -4
+KDA_ERR_DEVICE_TIMEOUT = -5
+KDA_ERR_CUDA = -6
+KDA_ERR_UNSUPPORTED_SHAPE = -7
+
+PATHS = {"auto": 0, "simt": 1, "tc": 2}
+DTYPES = {torch.bfloat16: 0, torch.float32: 1}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (code {code})")
+
+
+class _Args(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("theta", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("g_min", ctypes.c_float),
+                ("init_state", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("final_state", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
+                ("B", ctypes.c_int), ("H", ctypes.c_int), ("T", ctypes.c_int),
+                ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("path", ctypes.c_int)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libkda.so (building it first if needed).  Raises if impossible."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if build_if_missing:
+                path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"libkda.so not found at {path}; run __graft_entry__.build()")
+            lib = ctypes.CDLL(path)
+            vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            sig = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, vp]
+            for name in ("kda_chunk_fwd", "kda_chunk_fwd_f32"):
+                fn = getattr(lib, name)
+                fn.restype = i
+                fn.argtypes = sig
+            lib.kda_chunk_fwd_ex.restype = i
+            lib.kda_chunk_fwd_ex.argtypes = [ctypes.POINTER(_Args), vp]
+            lib.kda_device_status.restype = i
+            lib.kda_device_status.argtypes = [i]
+            lib.kda_select_path.restype = i
+            lib.kda_select_path.argtypes = [i, i, i]
+            lib.kda_strerror.restype = ctypes.c_char_p
+            lib.kda_strerror.argtypes = [i]
+            lib.kda_version.restype = i
+            lib.kda_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return load(build_if_missing=False).kda_strerror(int(code)).decode()
+    except Exception:  # pragma: no cover - used while reporting another error
+        return f"status {code}"
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torch.Tensor,
+                  beta: torch.Tensor, g_min: float = -5.0,
+                  init_state: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                  final_state: Optional[torch.Tensor] = None,
+                  cu_seqlens: Optional[torch.Tensor] = None, *, want_final_state: bool = True,
+                  path: str = "auto", stream=None):
+    """KDA chunked forward through the C ABI (``kda_chunk_fwd_ex``).
+
+    q, k, theta [B,T,H,dk]; v [B,T,H,dv]; beta [B,T,H], all bf16 or all fp32,
+    contiguous, on one CUDA device.  init_state/final_state fp32 [N,H,dk,dv]
+    (N = B, or the number of sequences when cu_seqlens [N+1] int32 is given
+    and B == 1).  Returns (out, final_state or None).  Asynchronous on
+    ``stream`` (default: torch's current stream).
+    """
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype = q.dtype
+    if dtype not in DTYPES:
+        raise TypeError(f"unsupported dtype {dtype}")
+    for name, t, shape in (("k", k, (B, T, H, dk)), ("theta", theta, (B, T, H, dk)),
+                           ("v", v, (B, T, H, dv)), ("beta", beta, (B, T, H))):
+        if t.dtype != dtype or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name}: expected contiguous {dtype} {shape}, got {t.dtype} "
+                             f"{tuple(t.shape)}")
+        if t.device != q.device:
+            raise ValueError(f"{name} on {t.device}, q on {q.device}")
+    if not q.is_cuda or not q.is_contiguous():
+        raise ValueError("q must be a contiguous CUDA tensor")
+    nseq = B
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("packed varlen input must have B == 1")
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise ValueError("cu_seqlens must be an int32 CUDA tensor")
+        nseq = cu_seqlens.numel() - 1
+    sshape = (nseq, H, dk, dv)
+    if init_state is not None:
+        if init_state.dtype != torch.float32 or tuple(init_state.shape) != sshape or \
+                not init_state.is_contiguous():
+            raise ValueError(f"init_state: expected contiguous fp32 {sshape}")
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=dtype, device=q.device)
+    if final_state is None and want_final_state:
+        final_state = torch.empty(sshape, dtype=torch.float32, device=q.device)
+    a = _Args(_ptr(q), _ptr(k), _ptr(v), _ptr(theta), _ptr(beta), float(g_min),
+              _ptr(init_state), _ptr(out), _ptr(final_state), _ptr(cu_seqlens),
+              nseq, H, T, dk, dv, DTYPES[dtype], PATHS[path])
+    with torch.cuda.device(q.device):
+        rc = lib.kda_chunk_fwd_ex(ctypes.byref(a), _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd_ex")
+    return out, final_state
+
+
+def kda_device_status(clear: bool = False) -> int:
+    return int(load().kda_device_status(1 if clear else 0))
+
+
+def kda_select_path(dtype: torch.dtype, dk: int, dv: int) -> str:
+    r = load().kda_select_path(DTYPES[dtype], dk, dv)
+    if r < 0:
+        raise KdaError(r, "kda_select_path")
+    return {v: k for k, v in PATHS.items()}[r]

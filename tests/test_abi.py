@@ -1,0 +1,83 @@
+"""The C ABI: the library builds and loads, exports every symbol include/kda.h
+declares, and rejects bad arguments on the host (no compute, no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_04_gb300 import kda as binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            with open(os.path.join(ROOT, "include", fn)) as f:
+                txt = f.read()
+            names += re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", txt)
+    return sorted(set(names))
+
+
+def test_header_declares_entry_points():
+    names = _declared_symbols()
+    for n in ("kda_chunk_fwd", "kda_chunk_fwd_f32", "kda_chunk_fwd_ex", "kda_device_status",
+              "kda_strerror", "kda_select_path", "kda_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = binding.load()
+    missing = [n for n in _declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_strerror_and_version():
+    lib = binding.load()
+    for code in range(-7, 1):
+        assert lib.kda_strerror(code)
+    assert lib.kda_strerror(-999) == b"unknown status code"
+    assert lib.kda_version() >= 100
+
+
+def _args(**over):
+    a = dict(q=0x1000, k=0x2000, v=0x3000, theta=0x4000, beta=0x5000, g_min=-5.0,
+             init_state=None, out=0x6000, final_state=None, cu_seqlens=None, B=1, H=1, T=16,
+             dk=128, dv=128, dtype=0, path=0)
+    a.update(over)
+    return binding._Args(**a)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(beta=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(out=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(B=0), binding.KDA_ERR_INVALID_ARG),
+    (dict(H=-1), binding.KDA_ERR_INVALID_ARG),
+    (dict(T=-5), binding.KDA_ERR_INVALID_ARG),
+    (dict(g_min=0.0), binding.KDA_ERR_INVALID_ARG),
+    (dict(g_min=1.0), binding.KDA_ERR_INVALID_ARG),
+    (dict(g_min=float("nan")), binding.KDA_ERR_INVALID_ARG),
+    (dict(dtype=7), binding.KDA_ERR_INVALID_ARG),
+    (dict(path=9), binding.KDA_ERR_INVALID_ARG),
+    (dict(dk=24), binding.KDA_ERR_UNSUPPORTED_SHAPE),
+    (dict(dv=256), binding.KDA_ERR_UNSUPPORTED_SHAPE),
+    (dict(q=0x1001), binding.KDA_ERR_MISALIGNED),
+    (dict(final_state=0x7004), binding.KDA_ERR_MISALIGNED),
+    (dict(cu_seqlens=0x8002), binding.KDA_ERR_MISALIGNED),
+])
+def test_host_side_rejection(over, code):
+    lib = binding.load()
+    a = _args(**over)
+    assert lib.kda_chunk_fwd_ex(ctypes.byref(a), None) == code
+    assert lib.kda_chunk_fwd_ex(None, None) == binding.KDA_ERR_INVALID_ARG
+
+
+def test_select_path_host_logic():
+    lib = binding.load()
+    assert lib.kda_select_path(1, 16, 16) == 1          # fp32 -> SIMT
+    assert lib.kda_select_path(0, 24, 128) == binding.KDA_ERR_UNSUPPORTED_SHAPE
+    assert lib.kda_select_path(5, 128, 128) == binding.KDA_ERR_INVALID_ARG
+    assert lib.kda_select_path(0, 64, 64) == 1          # bf16 off the TC shape -> SIMT
