@@ -54,12 +54,13 @@ def n_tokens(inp: dict) -> int:
     return int(sum(inp["lengths"]))
 
 
-def algorithmic_bytes(w: Workload, inp: dict) -> int:
+def algorithmic_bytes(w: Workload, inp: dict, out_bytes: int = 4) -> int:
     """Minimum HBM bytes of one pass: q, k, theta, v, beta read and out written
-    (e*(3dk+dv) + e + e*dv per token-head), plus the fp32 final state written
-    and the fp32 initial state read when given (4*dk*dv per chain each)."""
+    (e*(3dk+dv) + e + e_out*dv per token-head; out is fp32 by default), plus
+    the fp32 final state written and the fp32 initial state read when given
+    (4*dk*dv per chain each)."""
     e = torch.tensor([], dtype=w.dtype).element_size()
-    per = e * (3 * w.dk + w.dv) + e + e * w.dv
+    per = e * (3 * w.dk + w.dv) + e + out_bytes * w.dv
     chains = inp["N"] * w.H
     state = 4 * w.dk * w.dv * chains
     return token_heads(w, inp) * per + state * (2 if inp["init_state"] is not None else 1)
@@ -266,7 +267,7 @@ def run_ours(args, rank, world, local):
     q, k, v, th, be = inp["q"], inp["k"], inp["v"], inp["theta"], inp["beta"]
     init, cu = inp["init_state"], inp["cu_seqlens"]
     path = args.path if args.path != "auto" else kda_select_path(w.dtype, w.dk, w.dv)
-    out = torch.empty((q.shape[0], q.shape[1], w.H, w.dv), dtype=w.dtype, device=dev)
+    out = torch.empty((q.shape[0], q.shape[1], w.H, w.dv), dtype=torch.float32, device=dev)
     fin = torch.empty((inp["N"], w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -382,6 +383,7 @@ def run_ours(args, rank, world, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
             if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+            "out_dtype": "f32", "state_dtype": "f32",
             "config": {"workload": f"{w.name}: B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv}, "
                                    f"chunk 16, g_min={w.g_min}, fp32 state",
                        "B_per_gpu": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,

@@ -89,12 +89,19 @@ extern "C" {
 #define KDA_DTYPE_F32 1
 
 /*
- * kda_chunk_fwd -- bf16 q, k, v, theta, beta and out; fp32 states; fp32
- * arithmetic in the gate and the state, bf16 tensor-core operands.
+ * kda_chunk_fwd -- bf16 q, k, v, theta and beta; fp32 out; fp32 states.
+ * fp32 arithmetic in the gate, the cumulative sums and the state; bf16
+ * tensor-core operands with fp32 accumulation in the chunk products.
+ * `out` is fp32 because the outputs of this operator are heavy-tailed (the
+ * largest |o| is typically 14-18 times the RMS of o), so rounding even an
+ * exact result to bf16 already moves the largest entries by about 4e-2 of
+ * the RMS; an fp32 output keeps the error at the arithmetic's own level.
+ * (The pages keep attention outputs in FP32 too: "Kimi K3" explainer,
+ * section "Across the sequence".)  kda_chunk_fwd_ex can write bf16 instead.
  * Arguments as in the header comment above.  Returns KDA_OK or KDA_ERR_*.
  */
 KDA_API int kda_chunk_fwd(const void* q, const void* k, const void* v, const void* theta,
-                          const void* beta, float g_min, const float* init_state, void* out,
+                          const void* beta, float g_min, const float* init_state, float* out,
                           float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
                           int dk, int dv, cudaStream_t stream);
 
@@ -108,9 +115,12 @@ KDA_API int kda_chunk_fwd_f32(const float* q, const float* k, const float* v, co
                               float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
                               int dk, int dv, cudaStream_t stream);
 
-/* Extended call: the same operation with the dtype and the kernel path chosen
- * explicitly.  `dtype` is KDA_DTYPE_*; `path` is KDA_PATH_*.  KDA_PATH_TC
- * requires dtype bf16 and dk = dv = 128 (else KDA_ERR_UNSUPPORTED_SHAPE). */
+/* Extended call: the same operation with the element types and the kernel
+ * path chosen explicitly.  `dtype` (KDA_DTYPE_*) is the type of q, k, v,
+ * theta and beta; `out_dtype` that of out (KDA_DTYPE_F32, or KDA_DTYPE_BF16
+ * to halve the output bytes at the cost of bf16 rounding of o; fp32 inputs
+ * require an fp32 out).  `path` is KDA_PATH_*; KDA_PATH_TC requires bf16
+ * inputs and dk = dv = 128 (else KDA_ERR_UNSUPPORTED_SHAPE). */
 typedef struct kda_fwd_args {
   const void* q;
   const void* k;
@@ -124,6 +134,7 @@ typedef struct kda_fwd_args {
   const int32_t* cu_seqlens;
   int B, H, T, dk, dv;
   int dtype;
+  int out_dtype;
   int path;
 } kda_fwd_args;
 

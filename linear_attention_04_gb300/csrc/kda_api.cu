@@ -54,6 +54,8 @@ int validate(const kda_fwd_args* a) {
     return KDA_ERR_INVALID_ARG;
   if (!(a->g_min < 0.0f) || a->g_min != a->g_min) return KDA_ERR_INVALID_ARG;
   if (a->dtype != KDA_DTYPE_BF16 && a->dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+  if (a->out_dtype != KDA_DTYPE_BF16 && a->out_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+  if (a->dtype == KDA_DTYPE_F32 && a->out_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
   if (a->path != KDA_PATH_AUTO && a->path != KDA_PATH_SIMT && a->path != KDA_PATH_TC)
     return KDA_ERR_INVALID_ARG;
   if (!shape_ok(a->dk) || !shape_ok(a->dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
@@ -106,6 +108,7 @@ KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* a, cudaStream_t stream) {
   p.dk = a->dk;
   p.dv = a->dv;
   p.dtype = a->dtype;
+  p.out_dtype = a->out_dtype;
   if (empty && !a->cu_seqlens) {
     // no tokens: the final state is the initial state
     if (a->final_state) {
@@ -123,11 +126,11 @@ KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* a, cudaStream_t stream) {
 }
 
 KDA_API int kda_chunk_fwd(const void* q, const void* k, const void* v, const void* theta,
-                          const void* beta, float g_min, const float* init_state, void* out,
+                          const void* beta, float g_min, const float* init_state, float* out,
                           float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
                           int dk, int dv, cudaStream_t stream) {
   kda_fwd_args a{q, k, v, theta, beta, g_min, init_state, out, final_state, cu_seqlens,
-                 B, H, T, dk, dv, KDA_DTYPE_BF16, KDA_PATH_AUTO};
+                 B, H, T, dk, dv, KDA_DTYPE_BF16, KDA_DTYPE_F32, KDA_PATH_AUTO};
   return kda_chunk_fwd_ex(&a, stream);
 }
 
@@ -136,7 +139,7 @@ KDA_API int kda_chunk_fwd_f32(const float* q, const float* k, const float* v, co
                               float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
                               int dk, int dv, cudaStream_t stream) {
   kda_fwd_args a{q, k, v, theta, beta, g_min, init_state, out, final_state, cu_seqlens,
-                 B, H, T, dk, dv, KDA_DTYPE_F32, KDA_PATH_SIMT};
+                 B, H, T, dk, dv, KDA_DTYPE_F32, KDA_DTYPE_F32, KDA_PATH_SIMT};
   return kda_chunk_fwd_ex(&a, stream);
 }
 

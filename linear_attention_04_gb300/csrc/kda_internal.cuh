@@ -27,7 +27,8 @@ struct FwdParams {
   const int32_t* cu_seqlens;  // device, or nullptr for fixed length
   int N;                      // sequences (B for fixed length)
   int H, T, dk, dv;
-  int dtype;                  // KDA_DTYPE_*
+  int dtype;                  // KDA_DTYPE_* of q, k, v, theta, beta
+  int out_dtype;              // KDA_DTYPE_* of out
 };
 
 // Device status word of the current device (bounded waits write it).

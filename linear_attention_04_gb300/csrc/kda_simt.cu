@@ -45,12 +45,12 @@ struct SimtSmem {
   int rank_scratch[kMaxRankedSeqsDev + 1];
 };
 
-template <typename Tin, int DK, int DVS>
+template <typename Tin, typename Tout, int DK, int DVS>
 __global__ void __launch_bounds__(kSimtThreads)
     kda_fwd_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                         const Tin* __restrict__ v, const Tin* __restrict__ theta,
                         const Tin* __restrict__ beta, float g_min,
-                        const float* __restrict__ init_state, Tin* __restrict__ out,
+                        const float* __restrict__ init_state, Tout* __restrict__ out,
                         float* __restrict__ final_state, const int32_t* __restrict__ cu_seqlens,
                         int N, int H, int T, int dv) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kSimtThreads)
         float acc = 0.0f;
         for (int col = 0; col < DK; ++col) acc += sm.Qt[r][col] * sm.S[col][j];
         for (int s = 0; s <= r; ++s) acc += sm.P[r][s] * sm.V[s][j];
-        out[((c0 + r) * H + h) * (int64_t)dv + j0 + j] = from_f32<Tin>(acc);
+        out[((c0 + r) * H + h) * (int64_t)dv + j0 + j] = from_f32<Tout>(acc);
       }
     }
     __syncthreads();
@@ -213,9 +213,9 @@ __global__ void __launch_bounds__(kSimtThreads)
   }
 }
 
-template <typename Tin, int DK, int DVS>
+template <typename Tin, typename Tout, int DK, int DVS>
 int launch_simt_t(const FwdParams& p, cudaStream_t stream) {
-  auto kern = kda_fwd_simt_kernel<Tin, DK, DVS>;
+  auto kern = kda_fwd_simt_kernel<Tin, Tout, DK, DVS>;
   const size_t smem = sizeof(SimtSmem<DK, DVS>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
@@ -223,25 +223,25 @@ int launch_simt_t(const FwdParams& p, cudaStream_t stream) {
   dim3 grid((unsigned)(p.N * p.H), (unsigned)(p.dv / DVS));
   kern<<<grid, kSimtThreads, smem, stream>>>(
       (const Tin*)p.q, (const Tin*)p.k, (const Tin*)p.v, (const Tin*)p.theta, (const Tin*)p.beta,
-      p.g_min, p.init_state, (Tin*)p.out, p.final_state, p.cu_seqlens, p.N, p.H, p.T, p.dv);
+      p.g_min, p.init_state, (Tout*)p.out, p.final_state, p.cu_seqlens, p.N, p.H, p.T, p.dv);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
-template <typename Tin, int DK>
+template <typename Tin, typename Tout, int DK>
 int launch_simt_dk(const FwdParams& p, cudaStream_t stream) {
   switch (p.dv) {
-    case 16: return launch_simt_t<Tin, DK, 16>(p, stream);
-    default: return launch_simt_t<Tin, DK, 32>(p, stream);  // dv in {32, 64, 128}
+    case 16: return launch_simt_t<Tin, Tout, DK, 16>(p, stream);
+    default: return launch_simt_t<Tin, Tout, DK, 32>(p, stream);  // dv in {32, 64, 128}
   }
 }
 
-template <typename Tin>
+template <typename Tin, typename Tout>
 int launch_simt_dtype(const FwdParams& p, cudaStream_t stream) {
   switch (p.dk) {
-    case 16: return launch_simt_dk<Tin, 16>(p, stream);
-    case 32: return launch_simt_dk<Tin, 32>(p, stream);
-    case 64: return launch_simt_dk<Tin, 64>(p, stream);
-    case 128: return launch_simt_dk<Tin, 128>(p, stream);
+    case 16: return launch_simt_dk<Tin, Tout, 16>(p, stream);
+    case 32: return launch_simt_dk<Tin, Tout, 32>(p, stream);
+    case 64: return launch_simt_dk<Tin, Tout, 64>(p, stream);
+    case 128: return launch_simt_dk<Tin, Tout, 128>(p, stream);
     default: return KDA_ERR_UNSUPPORTED_SHAPE;
   }
 }
@@ -249,8 +249,9 @@ int launch_simt_dtype(const FwdParams& p, cudaStream_t stream) {
 }  // namespace
 
 int launch_simt(const FwdParams& p, cudaStream_t stream) {
-  if (p.dtype == KDA_DTYPE_F32) return launch_simt_dtype<float>(p, stream);
-  return launch_simt_dtype<__nv_bfloat16>(p, stream);
+  if (p.dtype == KDA_DTYPE_F32) return launch_simt_dtype<float, float>(p, stream);
+  if (p.out_dtype == KDA_DTYPE_BF16) return launch_simt_dtype<__nv_bfloat16, __nv_bfloat16>(p, stream);
+  return launch_simt_dtype<__nv_bfloat16, float>(p, stream);
 }
 
 }  // namespace kda

@@ -45,7 +45,7 @@ class _Args(ctypes.Structure):
                 ("final_state", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
                 ("B", ctypes.c_int), ("H", ctypes.c_int), ("T", ctypes.c_int),
                 ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("dtype", ctypes.c_int),
-                ("path", ctypes.c_int)]
+                ("out_dtype", ctypes.c_int), ("path", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -105,11 +105,12 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torc
                   init_state: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                   final_state: Optional[torch.Tensor] = None,
                   cu_seqlens: Optional[torch.Tensor] = None, *, want_final_state: bool = True,
-                  path: str = "auto", stream=None):
+                  out_dtype: torch.dtype = torch.float32, path: str = "auto", stream=None):
     """KDA chunked forward through the C ABI (``kda_chunk_fwd_ex``).
 
     q, k, theta [B,T,H,dk]; v [B,T,H,dv]; beta [B,T,H], all bf16 or all fp32,
-    contiguous, on one CUDA device.  init_state/final_state fp32 [N,H,dk,dv]
+    contiguous, on one CUDA device.  out [B,T,H,dv] is fp32 by default
+    (``out_dtype=torch.bfloat16`` is accepted for bf16 inputs).  init_state/final_state fp32 [N,H,dk,dv]
     (N = B, or the number of sequences when cu_seqlens [N+1] int32 is given
     and B == 1).  Returns (out, final_state or None).  Asynchronous on
     ``stream`` (default: torch's current stream).
@@ -142,12 +143,14 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torc
                 not init_state.is_contiguous():
             raise ValueError(f"init_state: expected contiguous fp32 {sshape}")
     if out is None:
-        out = torch.empty((B, T, H, dv), dtype=dtype, device=q.device)
+        out = torch.empty((B, T, H, dv), dtype=out_dtype, device=q.device)
+    elif out.dtype != out_dtype or tuple(out.shape) != (B, T, H, dv) or not out.is_contiguous():
+        raise ValueError(f"out: expected contiguous {out_dtype} {(B, T, H, dv)}")
     if final_state is None and want_final_state:
         final_state = torch.empty(sshape, dtype=torch.float32, device=q.device)
     a = _Args(_ptr(q), _ptr(k), _ptr(v), _ptr(theta), _ptr(beta), float(g_min),
               _ptr(init_state), _ptr(out), _ptr(final_state), _ptr(cu_seqlens),
-              nseq, H, T, dk, dv, DTYPES[dtype], PATHS[path])
+              nseq, H, T, dk, dv, DTYPES[dtype], DTYPES[out_dtype], PATHS[path])
     with torch.cuda.device(q.device):
         rc = lib.kda_chunk_fwd_ex(ctypes.byref(a), _stream_ptr(stream))
     if rc != KDA_OK:

@@ -45,7 +45,7 @@ def test_strerror_and_version():
 def _args(**over):
     a = dict(q=0x1000, k=0x2000, v=0x3000, theta=0x4000, beta=0x5000, g_min=-5.0,
              init_state=None, out=0x6000, final_state=None, cu_seqlens=None, B=1, H=1, T=16,
-             dk=128, dv=128, dtype=0, path=0)
+             dk=128, dv=128, dtype=0, out_dtype=1, path=0)
     a.update(over)
     return binding._Args(**a)
 
@@ -61,6 +61,8 @@ def _args(**over):
     (dict(g_min=1.0), binding.KDA_ERR_INVALID_ARG),
     (dict(g_min=float("nan")), binding.KDA_ERR_INVALID_ARG),
     (dict(dtype=7), binding.KDA_ERR_INVALID_ARG),
+    (dict(out_dtype=3), binding.KDA_ERR_INVALID_ARG),
+    (dict(dtype=1, out_dtype=0), binding.KDA_ERR_INVALID_ARG),
     (dict(path=9), binding.KDA_ERR_INVALID_ARG),
     (dict(dk=24), binding.KDA_ERR_UNSUPPORTED_SHAPE),
     (dict(dv=256), binding.KDA_ERR_UNSUPPORTED_SHAPE),

@@ -175,6 +175,25 @@ def test_null_states_and_continuation(path):
         assert_close(f64(Sb), f64(S_full), tol, "continuation state")
 
 
+@pytest.mark.parametrize("path", _bf16_paths())
+def test_bf16_output_option(path):
+    """bf16 out (opt-in): equal to the fp32-out result rounded to bf16 up to one
+    bf16 ulp, and within 2e-2 RMS + one bf16 ulp of |o| of the oracle."""
+    w, inp = _custom(B=1, H=3, T=70, init=0.2, seed=8)
+    g = _to(inp, "cuda")
+    o32, _ = _run(g, path)
+    o16, _ = kda_chunk_fwd(g["q"], g["k"], g["v"], g["theta"], g["beta"], -5.0, g["init_state"],
+                           out_dtype=torch.bfloat16, path=path)
+    torch.cuda.synchronize()
+    assert o16.dtype == torch.bfloat16
+    ref_o, _ = oracle_full(inp)
+    got = f64(o16)
+    ulp = np.abs(ref_o) * 2.0 ** -8
+    rms = float(np.sqrt(np.mean(ref_o ** 2)))
+    assert np.all(np.abs(got - ref_o) <= 2e-2 * rms + ulp)
+    assert np.all(np.abs(got - f64(o32)) <= np.abs(f64(o32)) * 2.0 ** -8 + 1e-30)
+
+
 def test_empty_sequence_batch():
     w, inp = _custom(B=2, H=2, T=0, init=0.5, seed=3)
     g = _to(inp, "cuda")
