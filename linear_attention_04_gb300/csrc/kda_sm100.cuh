@@ -242,5 +242,48 @@ KDA_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// ---------------------------------------------------------------- scalar MUFU ops
+// Hardware base-2 exponential and reciprocal (approximate forms, ~1-2 ulp).
+KDA_DEV float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+KDA_DEV float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------- packed fp32 pairs
+// Two fp32 values in one 64-bit register (low half = first element), operated on
+// with the sm_100 packed f32x2 instructions.
+typedef uint64_t f32x2;
+KDA_DEV f32x2 f2(float lo, float hi) {
+  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+KDA_DEV float f2lo(f32x2 v) { return __uint_as_float((uint32_t)v); }
+KDA_DEV float f2hi(f32x2 v) { return __uint_as_float((uint32_t)(v >> 32)); }
+KDA_DEV f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+KDA_DEV f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+KDA_DEV f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// bf16 pair (low element in the low 16 bits) -> two fp32 (exact)
+KDA_DEV f32x2 bf2_to_f2(uint32_t w) {
+  return (uint64_t)(w << 16) | ((uint64_t)(w & 0xffff0000u) << 32);
+}
+KDA_DEV uint32_t f2_to_bf2(f32x2 v) { return pack_bf16x2(f2lo(v), f2hi(v)); }
+
 }  // namespace sm100
 }  // namespace kda

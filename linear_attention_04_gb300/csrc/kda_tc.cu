@@ -13,31 +13,41 @@
 // "The Design" -- so the diagonal tile takes the same dense product path as
 // every other tile):
 //
-//   A   = strict_lower(Diag(beta) Kt Kh^T)      P = lower_incl_diag(Qt Kh^T)
+//   A   = strict_lower(Diag(beta) Kt Kh^T)      P = strict_lower(Qt Kh^T)
 //   Tb  = (I + A)^{-1} Diag(beta)               W = Tb Kt
-//   U   = Tb V - W S                            O = Qt S + P U
+//   U   = Tb V - W S                            O = Qt S + P U + Diag(q_t . k_t) U
 //   S  <- Diag(e^{G_C}) S + KhC^T U
 //
-// Warp roles (320 threads):
-//   warp 0        TMA producer: q, k, theta, v tiles of each chunk into a
-//                 2-stage ring (one lane); owns the TMEM allocation.
-//   warp 1        tcgen05.mma issuer (one lane).
-//   warps 2..5    "intra": gate g = g_min*sigmoid(theta) and cumulative sum in
-//                 fp32, the decayed bf16 operands, V^T into TMEM; then per
-//                 chunk the triangular inverse (fp32 forward substitution),
-//                 Tb, P, and W = Tb Kt (warp-level mma.sync, 16x128x16).
-//                 The A/P tiles of four chunks come from ONE tcgen05 MMA
-//                 (M = 128 rows = [Kt_c; Qt_c] for c = 0..3, N = 64 = Kh of the
-//                 four chunks); each chunk keeps its own 16 x 16 diagonal block.
-//   warps 6..9    "state": U readout, the per-chunk state pass (bf16 copy for
-//                 the next chunk's products, fp32 state scaled by e^{G_C}),
-//                 output and final-state stores.
+// The diagonal of Qt Kh^T is q_t . k_t exactly (the decay factors cancel), so
+// it is taken in fp32 from the bf16 inputs and applied to U in fp32; every
+// other product uses bf16 operands with fp32 accumulation, U as a bf16
+// high/low pair.  (The outputs are heavy-tailed -- max |o| is ~15x RMS -- and
+// the largest ones are dominated by the token's own term, which this keeps in
+// fp32.)
+//
+// Warp roles (256 threads, two warps per SM sub-partition):
+//   warps 0..3   state group: the sequential chain.  One elected lane issues
+//                the chain's tcgen05.mma; hand-offs inside the group are named
+//                barriers.  Per chunk: U readout, state/output products,
+//                state pass (bf16 copy first, then the fp32 state scaled by
+//                e^{G_C} of the next chunk), outputs, final state.
+//                Warp 0 owns the TMEM allocation.
+//   warps 4..7   intra group: TMA loads of q, k, theta, v tiles into a 4-stage
+//                ring (one lane refills a stage as soon as the group has
+//                consumed it); gate g = g_min*sigmoid(theta), cumulative sum
+//                and decayed operands in fp32 (two channels per thread, packed
+//                f32x2 arithmetic), V^T into TMEM, q.k diagonals; one lane
+//                issues the A/P product of four chunks (M = 128 rows =
+//                [Kt_c; Qt_c] for c = 0..3, N = 64 = Kh of the four chunks);
+//                then per chunk the triangular inverse (fp32 forward
+//                substitution), Tb, P and W = Tb Kt (warp-level mma.sync).
 //
 // Tensor-core products per chunk (M = 128 = dv lanes, K-major operands):
-//   [U' | 0]  = V^T [Tb | 0]^T           (A = V^T in TMEM, N = 32, K = 16)
-//   [U  | O] += S^T [-W | Qt]^T          (A = bf16 S^T in TMEM, N = 32, K = 128)
-//   S^T      += U^T KhC                  (A = bf16 U^T in TMEM, N = 128, K = 16)
-//   O        += U^T P^T                  (N = 16, K = 16)
+//   [U' | 0]   = V^T [Tb | 0]^T          (A = V^T in TMEM, N = 32, K = 16)
+//   [U  | O]  += S^T [-W | Qt]^T         (A = bf16 S^T in TMEM, N = 32, K = 128,
+//                                         two accumulators of K = 64 each)
+//   S^T       += U^T KhC                 (A = bf16 U^T hi and lo, N = 128, K = 16)
+//   O         += U^T P^T                 (N = 16, K = 16)
 //
 // Every wait is bounded: a wait that runs out sets the CTA's abort flag and the
 // device status word (KDA_ERR_DEVICE_TIMEOUT); every role then leaves its loop,
@@ -58,61 +68,61 @@ namespace {
 
 using namespace sm100;
 
-constexpr int C = kChunk;                 // 16
-constexpr int D = 128;                    // dk = dv
-constexpr int NS = 2;                     // TMA ring stages (one chunk each)
-constexpr int NSLOT = 8;                  // per-chunk operand slots (two groups)
-constexpr int kThreads = 320;
+constexpr int C = kChunk;                    // 16
+constexpr int D = 128;                       // dk = dv
+constexpr int NS = 4;                        // TMA ring stages (one chunk each)
+constexpr int NSLOT = 8;                     // per-chunk operand slots (two groups)
+constexpr int kThreads = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
+constexpr float kLog2e = 1.4426950408889634f;
 
 // tensor memory columns (512 allocated)
 constexpr uint32_t TM_S = 0;      // fp32 S^T, 128 columns
 constexpr uint32_t TM_SBF = 128;  // bf16 S^T (A operand), 64 columns
 constexpr uint32_t TM_AP = 192;   // A/P tiles of a group of 4 chunks, 64 columns
-constexpr uint32_t TM_UO = 256;   // [U | O] accumulators, 2 buffers x 32 columns
-constexpr uint32_t TM_UBF = 320;  // bf16 U^T (A operand): high part 8 columns, low part 8
-constexpr uint32_t TM_VT = 336;   // bf16 V^T (A operand), NSLOT buffers x 8 columns
+constexpr uint32_t TM_UA = 256;   // [U | O] accumulator A (K = 0..63), 2 buffers x 32
+constexpr uint32_t TM_UB = 320;   // [U | O] accumulator B (K = 64..127), 2 buffers x 32
+constexpr uint32_t TM_UBF = 384;  // bf16 U^T (A operand): high 8 columns, low 8 columns
+constexpr uint32_t TM_VT = 400;   // bf16 V^T (A operand), NSLOT buffers x 8 columns
 constexpr uint32_t TM_COLS = 512;
 static_assert(TM_VT + 8 * NSLOT <= TM_COLS, "tensor memory budget");
 
 // shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t TILE = C * D * 2;                       // 4096: one 16 x 128 bf16 tile
-constexpr uint32_t SM_RING = 0;                            // NS x {q, k, theta, v}
-constexpr uint32_t SM_GA = SM_RING + NS * 4 * TILE;        // 2 x [128 x 128] bf16, SW128
+constexpr uint32_t TILE = C * D * 2;                     // 4096: one 16 x 128 bf16 tile
+constexpr uint32_t SM_RING = 0;                          // NS x {q, k, theta, v}
+constexpr uint32_t SM_GA = SM_RING + NS * 4 * TILE;      // 2 x [128 x 128] bf16, SW128
 constexpr uint32_t GA_BYTES = 128 * D * 2;
-constexpr uint32_t SM_GAL = SM_GA + 2 * GA_BYTES;          // [128 x 128] bf16 low parts
-constexpr uint32_t SM_GB = SM_GAL + GA_BYTES;              // [64 x 128] bf16, SW128
+constexpr uint32_t SM_GB = SM_GA + 2 * GA_BYTES;         // [64 x 128] bf16, SW128
 constexpr uint32_t GB_BYTES = 64 * D * 2;
-constexpr uint32_t SM_GBL = SM_GB + GB_BYTES;              // [64 x 128] bf16 low parts
-constexpr uint32_t SM_KC = SM_GBL + GB_BYTES;              // NSLOT x [128 x 16] bf16
-constexpr uint32_t SM_P = SM_KC + NSLOT * TILE;            // NSLOT x 2 x [16 x 16] bf16 (hi, lo)
-constexpr uint32_t SM_TB = SM_P + NSLOT * 1024;            // NSLOT x [32 x 16] bf16
-constexpr uint32_t SM_EGC = SM_TB + NSLOT * 1024;          // NSLOT x 128 fp32
-constexpr uint32_t SM_BETA = SM_EGC + NSLOT * D * 4;       // NSLOT x 16 fp32
-constexpr uint32_t SM_ABUF = SM_BETA + NSLOT * C * 4;      // 4 warps x [16 x 17] fp32
-constexpr uint32_t SM_BARS = SM_ABUF + 4 * C * 17 * 4;     // mbarriers
-constexpr int NBARS = 40;
-constexpr uint32_t SM_MISC = SM_BARS + NBARS * 8;          // tmem base, abort flag
-constexpr uint32_t SM_RANK = SM_MISC + 16;                 // chain-order scratch
+constexpr uint32_t SM_KC = SM_GB + GB_BYTES;             // NSLOT x [128 x 16] bf16
+constexpr uint32_t SM_P = SM_KC + NSLOT * TILE;          // NSLOT x [16 x 16] bf16
+constexpr uint32_t SM_TB = SM_P + NSLOT * 512;           // NSLOT x [32 x 16] bf16
+constexpr uint32_t SM_EGC = SM_TB + NSLOT * 1024;        // NSLOT x 128 fp32
+constexpr uint32_t SM_BETA = SM_EGC + NSLOT * D * 4;     // NSLOT x 16 fp32
+constexpr uint32_t SM_DIAG = SM_BETA + NSLOT * C * 4;    // NSLOT x 4 warps x 16 fp32
+constexpr uint32_t SM_ABUF = SM_DIAG + NSLOT * 4 * C * 4;  // 4 warps x [16 x 17] fp32
+constexpr uint32_t SM_BARS = SM_ABUF + 4 * C * 17 * 4;   // mbarriers
+constexpr int NBARS = 48;
+constexpr uint32_t SM_MISC = SM_BARS + NBARS * 8;        // tmem base, abort flag
+constexpr uint32_t SM_RANK = SM_MISC + 16;               // chain-order scratch
 constexpr uint32_t SM_TOTAL = SM_RANK + (kMaxRankedSeqsDev + 1) * 4;
-constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;           // + alignment slack
+constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;         // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(SM_GA % 1024 == 0 && SM_GAL % 1024 == 0 && SM_GB % 1024 == 0 && SM_GBL % 1024 == 0,
-              "SW128 tiles must be 1024-aligned");
+static_assert(SM_GA % 1024 == 0 && SM_GB % 1024 == 0, "SW128 tiles must be 1024-aligned");
 
 // barrier indices
-constexpr int B_FULL = 0;          // [NS]  TMA -> intra
-constexpr int B_EMPTY = 4;         // [NS]  intra -> TMA
-constexpr int B_GATE = 8;          // [8]   intra (gate/operands of chunk n) -> state warps
-constexpr int B_CHUNK = 16;        // [8]   intra (W, Tb, P of chunk n) -> MMA
-constexpr int B_OPS = 24;          // [2]   intra (operands of a group) -> MMA (A/P product)
-constexpr int B_GFREE = 26;        // [2]   MMA (group done) -> intra
-constexpr int B_APDONE = 30;       //       MMA (A/P product done) -> intra
-constexpr int B_UREADY = 31;       //       MMA (U, O products done) -> state warps
-constexpr int B_UBF = 32;          //       state warps (bf16 U^T written) -> MMA
-constexpr int B_SODONE = 33;       //       MMA (state and output products done) -> state warps
-constexpr int B_STATE = 34;        //       state warps (state pass done) -> MMA
-constexpr int B_DRAIN = 35;        //       MMA final drain
+constexpr int B_FULL = 0;     // [NS]    TMA -> intra
+constexpr int B_GATE = 8;     // [NSLOT] intra phase A of chunk n done -> state group
+constexpr int B_CHUNK = 16;   // [NSLOT] intra phase B of chunk n done -> state issuer
+constexpr int B_GFREE = 24;   // [2]     state issuer: group's products done -> intra
+constexpr int B_APDONE = 26;  //         A/P product done -> intra
+constexpr int B_X = 27;       //         [U | O] products of chunk n done -> state group
+constexpr int B_SO = 28;      //         state and output products of chunk n done
+constexpr int B_DRAIN = 29;   //         state issuer final drain
+constexpr int B_DRAIN2 = 30;  //         intra issuer final drain
+
+// named barriers
+constexpr uint32_t NB_INTRA = 1, NB_STATE = 2;
 
 // byte offset of element (row, col) in a SW128 K-major tile with `rows` rows
 __device__ __forceinline__ uint32_t sw128(int row, int col, int rows) {
@@ -135,10 +145,11 @@ struct TcArgs {
 // Optional event trace of the first CTA (compile with -DKDA_TRACE): wall-clock
 // time of each pipeline event per chunk, read back with kda_debug_trace_read.
 constexpr int kTraceChunks = 512;
+static_assert(kTraceChunks > 0, "trace size");
 #ifdef KDA_TRACE
 __device__ unsigned long long g_kda_trace[kTraceChunks * 16];
-#define KTRACE(n, k)                                                   \
-  do {                                                                 \
+#define KTRACE(n, k)                                                                          \
+  do {                                                                                        \
     if (blockIdx.x == 0 && (n) < kTraceChunks) g_kda_trace[(n) * 16 + (k)] = globaltimer_ns(); \
   } while (0)
 #else
@@ -173,11 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ngroups = (nchunks + 3) / 4;
 
   if (tid == 0) {
-    for (int i = 0; i < NBARS; ++i) {
-      uint32_t cnt = 1;
-      if (i == B_UBF || i == B_STATE) cnt = 4;
-      mbar_init(&bars[i], cnt);
-    }
+    for (int i = 0; i < NBARS; ++i) mbar_init(&bars[i], 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -190,146 +197,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     __syncwarp();
     tmem_alloc(tmem_slot, TM_COLS);
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_th);
-      prefetch_tmap(&tm_v);
-    }
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t sbase = smem_u32(sm);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int issued = 0;
-      for (int n = 0; n < nchunks; ++n) {
-        const int s = n % NS;
-        if (n >= NS && !mbar_wait(&bars[B_EMPTY + s], ((n / NS) - 1) & 1, abort, kWaitNs)) {
-          fail(abort, args.status);
-          break;
-        }
-        mbar_arrive_expect_tx(&bars[B_FULL + s], 4 * TILE);
-        KTRACE(n, 0);
-        unsigned char* st = sm + SM_RING + s * 4 * TILE;
-        const int row = (int)(ch.t0 + (int64_t)n * C);
-        tma_load_3d(st + 0 * TILE, &tm_q, 0, h, row, &bars[B_FULL + s]);
-        tma_load_3d(st + 1 * TILE, &tm_k, 0, h, row, &bars[B_FULL + s]);
-        tma_load_3d(st + 2 * TILE, &tm_th, 0, h, row, &bars[B_FULL + s]);
-        tma_load_3d(st + 3 * TILE, &tm_v, 0, h, row, &bars[B_FULL + s]);
-        issued = n + 1;
-      }
-      // drain: every issued load has landed before the CTA may exit
-      for (int n = issued - NS < 0 ? 0 : issued - NS; n < issued; ++n)
-        mbar_wait_drain(&bars[B_FULL + n % NS], (n / NS) & 1, kWaitNs);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nchunks > 0) {
-      const uint32_t sbase = smem_u32(sm);
-      int ap_next = 0;
-      // A/P tiles of group g: [Kt;Qt] Kh^T with the P rows to ~16-bit precision:
-      // hi*hi + hi*lo + lo*hi, every product accumulated in fp32
-      auto issue_ap = [&](int g) {
-        const uint32_t ga = sbase + SM_GA + (g & 1) * GA_BYTES, gal = sbase + SM_GAL;
-        const uint32_t gb = sbase + SM_GB, gbl = sbase + SM_GBL;
-#pragma unroll
-        for (int pass = 0; pass < 3; ++pass) {
-          const uint32_t aa = pass == 2 ? gal : ga, bb = pass == 1 ? gbl : gb;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            uint64_t a = sdesc_sw128(aa + (kk >> 2) * (128 * 128) + (kk & 3) * 32);
-            uint64_t b = sdesc_sw128(bb + (kk >> 2) * (64 * 128) + (kk & 3) * 32);
-            mma_ss(tmem + TM_AP, a, b, idesc_bf16_f32(128, 64), (pass > 0) || (kk > 0));
-          }
-        }
-        mma_commit(&bars[B_APDONE]);
-      };
-      auto try_issue_ap = [&]() {
-        if (ap_next < ngroups && mbar_try_wait(&bars[B_OPS + (ap_next & 1)], (ap_next >> 1) & 1)) {
-          tc_fence_after();
-          issue_ap(ap_next);
-          KTRACE(4 * ap_next, 15);
-          ++ap_next;
-        }
-      };
-      // wait that keeps issuing the next group's A/P product while it waits
-      auto wait_poll = [&](uint64_t* bar, uint32_t parity) -> bool {
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t it = 0;; ++it) {
-          if (mbar_try_wait(bar, parity)) return true;
-          try_issue_ap();
-          if ((it & 31u) == 31u) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitNs) return false;
-          }
-        }
-      };
-      bool ok = true;
-      for (int n = 0; n < nchunks && ok; ++n) {
-        const int g = n >> 2, cc = n & 3, slot = n % NSLOT, buf = n & 1;
-        while (ap_next <= g) {
-          if (!mbar_wait(&bars[B_OPS + (ap_next & 1)], (ap_next >> 1) & 1, abort, kWaitNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_ap(ap_next);
-          KTRACE(4 * ap_next, 15);
-          ++ap_next;
-        }
-        if (!ok) break;
-        if (!wait_poll(&bars[B_CHUNK + slot], (n / NSLOT) & 1)) { ok = false; break; }
-        KTRACE(n, 5);
-        tc_fence_after();
-        const uint32_t uo = tmem + TM_UO + 32 * buf;
-        // [U' | 0] = V^T [Tb | 0]^T
-        mma_ts(uo, tmem + TM_VT + 8 * slot, sdesc_noswz(sbase + SM_TB + slot * 1024, 512, 128),
-               idesc_bf16_f32(128, 32), 0);
-        if (!wait_poll(&bars[B_STATE], n & 1)) { ok = false; break; }
-        KTRACE(n, 6);
-        tc_fence_after();
-        // [U | O] += S^T [-W | Qt]^T
-        const uint32_t ga = sbase + SM_GA + (g & 1) * GA_BYTES + cc * 32 * 128;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          uint64_t b = sdesc_sw128(ga + (kk >> 2) * (128 * 128) + (kk & 3) * 32);
-          mma_ts(uo, tmem + TM_SBF + 8 * kk, b, idesc_bf16_f32(128, 32), 1);
-        }
-        mma_commit(&bars[B_UREADY]);
-        KTRACE(n, 7);
-        if (!wait_poll(&bars[B_UBF], n & 1)) { ok = false; break; }
-        KTRACE(n, 8);
-        tc_fence_after();
-        // S^T += (U_hi + U_lo)^T KhC ;  O += U^T P^T as hi*hi + hi*lo + lo*hi
-        {
-          const uint64_t kc = sdesc_noswz(sbase + SM_KC + slot * TILE, 2048, 128);
-          const uint64_t ph = sdesc_noswz(sbase + SM_P + slot * 1024, 256, 128);
-          const uint64_t pl = sdesc_noswz(sbase + SM_P + slot * 1024 + 512, 256, 128);
-          mma_ts(tmem + TM_S, tmem + TM_UBF, kc, idesc_bf16_f32(128, 128), 1);
-          mma_ts(tmem + TM_S, tmem + TM_UBF + 8, kc, idesc_bf16_f32(128, 128), 1);
-          mma_ts(uo + 16, tmem + TM_UBF, ph, idesc_bf16_f32(128, 16), 1);
-          mma_ts(uo + 16, tmem + TM_UBF, pl, idesc_bf16_f32(128, 16), 1);
-          mma_ts(uo + 16, tmem + TM_UBF + 8, ph, idesc_bf16_f32(128, 16), 1);
-        }
-        mma_commit(&bars[B_SODONE]);
-        KTRACE(n, 9);
-        if (cc == 3 || n == nchunks - 1) mma_commit(&bars[B_GFREE + (g & 1)]);
-      }
-      if (!ok) fail(abort, args.status);
-      // drain every MMA this thread issued
-      mma_commit(&bars[B_DRAIN]);
-      mbar_wait_drain(&bars[B_DRAIN], 0, kWaitNs);
-    }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ intra warps
-    const int it = tid - 64;          // 0..127: key/value channel of this thread in phase A
+  if (warp >= 4) {
+    // ================================================================ intra group
+    const int it = tid - 128;         // 0..127
     const int q4 = warp & 3;          // TMEM lane quarter of this warp
-    const int dvq = q4 * 32 + lane;   // value channel this thread moves into V^T
+    const int wq = warp - 4;          // warp index inside the group
+    const int cp = it >> 1;           // channel pair: channels 2cp, 2cp+1
+    const int hf = it & 1;            // token half: rows 8hf .. 8hf+7
+    const f32x2 kC2 = f2(-kLog2e, -kLog2e);
+    const f32x2 kC1 = f2(args.g_min * kLog2e, args.g_min * kLog2e);
+    const f32x2 kOne = f2(1.0f, 1.0f);
+    const f32x2 kZero = 0ull;
+    // TMA loads of chunk m into ring stage m % NS (issued by one lane)
+    auto load_chunk = [&](int m) {
+      const int s = m % NS;
+      mbar_arrive_expect_tx(&bars[B_FULL + s], 4 * TILE);
+      KTRACE(m, 0);
+      unsigned char* st = sm + SM_RING + s * 4 * TILE;
+      const int row = (int)(ch.t0 + (int64_t)m * C);
+      tma_load_3d(st + 0 * TILE, &tm_q, 0, h, row, &bars[B_FULL + s]);
+      tma_load_3d(st + 1 * TILE, &tm_k, 0, h, row, &bars[B_FULL + s]);
+      tma_load_3d(st + 2 * TILE, &tm_th, 0, h, row, &bars[B_FULL + s]);
+      tma_load_3d(st + 3 * TILE, &tm_v, 0, h, row, &bars[B_FULL + s]);
+    };
+    int issued = 0;
+    if (it == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_th);
+      prefetch_tmap(&tm_v);
+      for (; issued < NS && issued < nchunks; ++issued) load_chunk(issued);
+    }
     bool bad = false;
     for (int g = 0; g < ngroups; ++g) {
       const int gb = g & 1;
@@ -346,76 +252,158 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it == 0) KTRACE(n, 1);
         const int nvalid = min(C, L - n * C);
         const unsigned char* st = sm + SM_RING + s * 4 * TILE;
-        const __nv_bfloat16* sq = (const __nv_bfloat16*)(st + 0 * TILE);
-        const __nv_bfloat16* sk = (const __nv_bfloat16*)(st + 1 * TILE);
-        const __nv_bfloat16* sth = (const __nv_bfloat16*)(st + 2 * TILE);
-        const __nv_bfloat16* sv = (const __nv_bfloat16*)(st + 3 * TILE);
-        float G = 0.0f, Gr[C], kr[C];
+        const uint32_t* sq = (const uint32_t*)(st + 0 * TILE);
+        const uint32_t* sk = (const uint32_t*)(st + 1 * TILE);
+        const uint32_t* sth = (const uint32_t*)(st + 2 * TILE);
+        const uint32_t* sv = (const uint32_t*)(st + 3 * TILE);
+        f32x2 Gr[8], kr[8], qr[8];
+        uint32_t vw[8];
+        f32x2 G2 = kZero;
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
+        for (int i = 0; i < 8; ++i) {
+          const int r = 8 * hf + i;
           const bool valid = r < nvalid;
-          const float th = __bfloat162float(sth[r * D + it]);
-          const float kv = valid ? __bfloat162float(sk[r * D + it]) : 0.0f;
-          const float qv = valid ? __bfloat162float(sq[r * D + it]) : 0.0f;
-          const float gg = valid ? args.g_min * (1.0f / (1.0f + __expf(-th))) : 0.0f;
-          G += gg;
-          Gr[r] = G;
-          kr[r] = kv;
-          const float eg = __expf(G), emg = __expf(-G);
-          const float xk = kv * eg, xq = qv * eg, xh = kv * emg;
-          const __nv_bfloat16 hk = __float2bfloat16_rn(xk), hq = __float2bfloat16_rn(xq),
-                              hh = __float2bfloat16_rn(xh);
-          const uint32_t oa = sw128(32 * cc + r, it, 128), oq = sw128(32 * cc + 16 + r, it, 128);
-          const uint32_t ob = sw128(16 * cc + r, it, 64);
-          *(__nv_bfloat16*)(GA + oa) = hk;
-          *(__nv_bfloat16*)(GA + oq) = hq;
-          *(__nv_bfloat16*)(sm + SM_GAL + oa) = __float2bfloat16_rn(xk - __bfloat162float(hk));
-          *(__nv_bfloat16*)(sm + SM_GAL + oq) = __float2bfloat16_rn(xq - __bfloat162float(hq));
-          *(__nv_bfloat16*)(sm + SM_GB + ob) = hh;
-          *(__nv_bfloat16*)(sm + SM_GBL + ob) = __float2bfloat16_rn(xh - __bfloat162float(hh));
+          const f32x2 th = bf2_to_f2(sth[r * 64 + cp]);
+          kr[i] = valid ? bf2_to_f2(sk[r * 64 + cp]) : kZero;
+          qr[i] = valid ? bf2_to_f2(sq[r * 64 + cp]) : kZero;
+          vw[i] = valid ? sv[r * 64 + cp] : 0u;
+          const f32x2 x = mul2(th, kC2);
+          const f32x2 den = add2(f2(ex2_approx(f2lo(x)), ex2_approx(f2hi(x))), kOne);
+          const f32x2 g2 = mul2(f2(rcp_approx(f2lo(den)), rcp_approx(f2hi(den))), kC1);
+          G2 = add2(G2, valid ? g2 : kZero);  // log2-domain cumulative log-decay
+          Gr[i] = G2;
+        }
+        // the second token half adds the first half's total; both need the chunk total
+        const f32x2 other =
+            ((uint64_t)__shfl_xor_sync(0xffffffffu, (uint32_t)(G2 >> 32), 1) << 32) |
+            (uint64_t)__shfl_xor_sync(0xffffffffu, (uint32_t)G2, 1);
+        if (hf) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) Gr[i] = add2(Gr[i], other);
+        }
+        const f32x2 GT = add2(G2, other);  // chunk total (same in both halves)
+        const f32x2 eGC = f2(ex2_approx(f2lo(GT)), ex2_approx(f2hi(GT)));
+        uint32_t kc0[4], kc1[4];
+        float dpart[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 8 * hf + i;
+          const f32x2 eg = f2(ex2_approx(f2lo(Gr[i])), ex2_approx(f2hi(Gr[i])));
+          const f32x2 emg = f2(ex2_approx(-f2lo(Gr[i])), ex2_approx(-f2hi(Gr[i])));
+          const f32x2 kt = mul2(kr[i], eg), qt = mul2(qr[i], eg), kh = mul2(kr[i], emg);
+          *(uint32_t*)(GA + sw128(32 * cc + r, 2 * cp, 128)) = f2_to_bf2(kt);
+          *(uint32_t*)(GA + sw128(32 * cc + 16 + r, 2 * cp, 128)) = f2_to_bf2(qt);
+          *(uint32_t*)(sm + SM_GB + sw128(16 * cc + r, 2 * cp, 64)) = f2_to_bf2(kh);
+          const f32x2 khc = mul2(kh, eGC);
+          if (i & 1) {
+            kc0[i >> 1] = pack_bf16x2(__uint_as_float(kc0[i >> 1]), f2lo(khc));
+            kc1[i >> 1] = pack_bf16x2(__uint_as_float(kc1[i >> 1]), f2hi(khc));
+          } else {
+            kc0[i >> 1] = __float_as_uint(f2lo(khc));
+            kc1[i >> 1] = __float_as_uint(f2hi(khc));
+          }
+          const f32x2 qk = mul2(qr[i], kr[i]);
+          dpart[i] = f2lo(qk) + f2hi(qk);
         }
         {
-          // KhC^T tile: row = key channel, 16 tokens along K (no swizzle)
-          uint32_t w[8];
+          // KhC^T tile: row = key channel, 16 tokens along K (no swizzle);
+          // this thread holds channels 2cp, 2cp+1 and tokens 8hf .. 8hf+7
+          unsigned char* kc = sm + SM_KC + slot * TILE + hf * 2048;
+          const int c0 = 2 * cp, c1 = 2 * cp + 1;
+          *(uint4*)(kc + (c0 & 7) * 16 + (c0 >> 3) * 128) = make_uint4(kc0[0], kc0[1], kc0[2], kc0[3]);
+          *(uint4*)(kc + (c1 & 7) * 16 + (c1 >> 3) * 128) = make_uint4(kc1[0], kc1[1], kc1[2], kc1[3]);
+          if (hf == 0)
+            *(float2*)(sm + SM_EGC + slot * D * 4 + c0 * 4) = make_float2(f2lo(eGC), f2hi(eGC));
+        }
+        {
+          // q_t . k_t over this warp's 32 channels: reduce 8 rows over the 16
+          // lanes of the same token half (lane bits 1..4), one row per lane
+          const int b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+          float v4[4], v2[2], v1;
 #pragma unroll
-          for (int p = 0; p < 8; ++p)
-            w[p] = pack_bf16x2(kr[2 * p] * __expf(G - Gr[2 * p]),
-                               kr[2 * p + 1] * __expf(G - Gr[2 * p + 1]));
-          unsigned char* kc = sm + SM_KC + slot * TILE + (it & 7) * 16 + (it >> 3) * 128;
-          *(uint4*)(kc) = make_uint4(w[0], w[1], w[2], w[3]);
-          *(uint4*)(kc + 2048) = make_uint4(w[4], w[5], w[6], w[7]);
-          ((float*)(sm + SM_EGC + slot * D * 4))[it] = __expf(G);
+          for (int j = 0; j < 4; ++j) {
+            const float send = b4 ? dpart[j] : dpart[j + 4];
+            const float keep = b4 ? dpart[j + 4] : dpart[j];
+            v4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+          }
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float send = b3 ? v4[j] : v4[j + 2];
+            const float keep = b3 ? v4[j + 2] : v4[j];
+            v2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+          }
+          {
+            const float send = b2 ? v2[0] : v2[1];
+            const float keep = b2 ? v2[1] : v2[0];
+            v1 = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+          }
+          v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+          if ((lane & 2) == 0) {
+            const int row = 8 * hf + 4 * b4 + 2 * b3 + b2;
+            ((float*)(sm + SM_DIAG + slot * 4 * C * 4))[wq * C + row] = v1;
+          }
         }
         if (it < C) {
-          const float b = it < nvalid ? __bfloat162float(args.beta[(ch.t0 + (int64_t)n * C + it) * H + h])
-                                      : 0.0f;
+          const float b = it < nvalid
+                              ? __bfloat162float(args.beta[(ch.t0 + (int64_t)n * C + it) * H + h])
+                              : 0.0f;
           ((float*)(sm + SM_BETA + slot * C * 4))[it] = b;
         }
         {
-          // V^T into tensor memory: lane = value channel, 16 tokens packed in 8 columns
-          __syncwarp();
+          // V^T into tensor memory: TMEM lane = value channel 32*q4 + lane.  This
+          // thread holds channels {lane & ~1, lane | 1} (of this warp's 32) for
+          // 8 tokens; it swaps the partner's channel with the partner.
+          uint32_t mine[4], give[4];
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const uint32_t a = vw[2 * p], b = vw[2 * p + 1];  // tokens 2p, 2p+1 of this half
+            const uint32_t lo = __byte_perm(a, b, 0x5410);    // channel 2cp   of both tokens
+            const uint32_t hi = __byte_perm(a, b, 0x7632);    // channel 2cp+1 of both tokens
+            mine[p] = (lane & 1) ? hi : lo;
+            give[p] = (lane & 1) ? lo : hi;
+          }
           uint32_t w[8];
 #pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            float v0 = (2 * p < nvalid) ? __bfloat162float(sv[(2 * p) * D + dvq]) : 0.0f;
-            float v1 = (2 * p + 1 < nvalid) ? __bfloat162float(sv[(2 * p + 1) * D + dvq]) : 0.0f;
-            w[p] = pack_bf16x2(v0, v1);
+          for (int p = 0; p < 4; ++p) {
+            const uint32_t got = __shfl_xor_sync(0xffffffffu, give[p], 1);
+            w[4 * hf + p] = mine[p];
+            w[4 * (1 - hf) + p] = got;
           }
+          __syncwarp();
           tmem_st_x8(tmem + ((uint32_t)(q4 * 32) << 16) + TM_VT + 8 * slot, w);
           tmem_wait_st();
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        if (bar_sync_or(1, 128, bad || *abort)) { stop = true; break; }
+        if (bar_sync_or(NB_INTRA, 128, bad || *abort)) {
+          stop = true;
+          break;
+        }
         if (it == 0) {
-          mbar_arrive(&bars[B_EMPTY + s]);
           mbar_arrive(&bars[B_GATE + slot]);
           KTRACE(n, 2);
+          if (n + NS < nchunks) {
+            // the whole group has consumed stage s: refill it
+            fence_proxy_async_smem();
+            load_chunk(n + NS);
+            issued = n + NS + 1;
+          }
         }
       }
       if (stop) break;
-      if (it == 0) mbar_arrive(&bars[B_OPS + gb]);
-
+      // ---- the group's A/P tiles in one product, issued by one lane
+      if (it == 0) {
+        tc_fence_after();
+        const uint32_t ga = sbase + SM_GA + gb * GA_BYTES, gbb = sbase + SM_GB;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint64_t a = sdesc_sw128(ga + (kk >> 2) * (128 * 128) + (kk & 3) * 32);
+          uint64_t b = sdesc_sw128(gbb + (kk >> 2) * (64 * 128) + (kk & 3) * 32);
+          mma_ss(tmem + TM_AP, a, b, idesc_bf16_f32(128, 64), kk > 0);
+        }
+        mma_commit(&bars[B_APDONE]);
+        KTRACE(4 * g, 11);
+      }
       // ---- phase B: this warp's chunk of the group (lane quarter q4 holds its A/P rows)
       const int n = 4 * g + q4;
       if (n < nchunks) {
@@ -429,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         float* Ab = (float*)(sm + SM_ABUF) + q4 * (C * 17);
         const float* bet = (const float*)(sm + SM_BETA + slot * C * 4);
-        unsigned char* Pt = sm + SM_P + slot * 1024;
+        unsigned char* Pt = sm + SM_P + slot * 512;
         unsigned char* Tb = sm + SM_TB + slot * 1024;
         if (lane < 16) {
           const int i = lane;
@@ -437,22 +425,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < C; ++j) Ab[i * 17 + j] = (j < i) ? bi * __uint_as_float(raw[j]) : 0.0f;
         } else {
+          // strictly lower P (the diagonal is applied exactly by the state group)
           const int i = lane - 16;
-          // P row i, split into a bf16 high part and a bf16 low part
-          uint32_t wh[8], wl[8];
+          uint32_t w[8];
 #pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            const float x0 = (2 * p <= i) ? __uint_as_float(raw[2 * p]) : 0.0f;
-            const float x1 = (2 * p + 1 <= i) ? __uint_as_float(raw[2 * p + 1]) : 0.0f;
-            wh[p] = pack_bf16x2(x0, x1);
-            const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&wh[p]);
-            wl[p] = pack_bf16x2(x0 - __low2float(hb), x1 - __high2float(hb));
-          }
+          for (int p = 0; p < 8; ++p)
+            w[p] = pack_bf16x2((2 * p < i) ? __uint_as_float(raw[2 * p]) : 0.0f,
+                               (2 * p + 1 < i) ? __uint_as_float(raw[2 * p + 1]) : 0.0f);
           unsigned char* pr = Pt + (i & 7) * 16 + (i >> 3) * 128;
-          *(uint4*)(pr) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-          *(uint4*)(pr + 256) = make_uint4(wh[4], wh[5], wh[6], wh[7]);
-          *(uint4*)(pr + 512) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-          *(uint4*)(pr + 768) = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+          *(uint4*)(pr) = make_uint4(w[0], w[1], w[2], w[3]);
+          *(uint4*)(pr + 256) = make_uint4(w[4], w[5], w[6], w[7]);
         }
         __syncwarp();
         if (lane < 16) {
@@ -505,68 +487,115 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t4 = 0; t4 < 4; ++t4) {
               const int col = 8 * (4 * grp + t4) + 2 * (lane & 3);
 #pragma unroll
-              for (int hf = 0; hf < 2; ++hf) {
-                const int R = 32 * q4 + (lane >> 2) + 8 * hf;
+              for (int hf2 = 0; hf2 < 2; ++hf2) {
+                const int R = 32 * q4 + (lane >> 2) + 8 * hf2;
                 *(uint32_t*)(GA + sw128(R, col, 128)) =
-                    pack_bf16x2(-acc[t4][2 * hf], -acc[t4][2 * hf + 1]);
+                    pack_bf16x2(-acc[t4][2 * hf2], -acc[t4][2 * hf2 + 1]);
               }
             }
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[B_CHUNK + slot]);
-        if (lane == 0) KTRACE(n, 4);
+        if (lane == 0) {
+          mbar_arrive(&bars[B_CHUNK + slot]);
+          KTRACE(n, 4);
+        }
       }
     }
     if (bad) fail(abort, args.status);
+    if (it == 0) {
+      // drain the A/P products this group issued, and every TMA load in flight
+      mma_commit(&bars[B_DRAIN2]);
+      mbar_wait_drain(&bars[B_DRAIN2], 0, kWaitNs);
+      for (int m = issued - NS < 0 ? 0 : issued - NS; m < issued; ++m)
+        mbar_wait_drain(&bars[B_FULL + m % NS], (m / NS) & 1, kWaitNs);
+    }
   } else {
-    // ------------------------------------------------------------ state warps
+    // ================================================================ state group
     const int q4 = warp & 3;
     const int dv = q4 * 32 + lane;
     const uint32_t lb = (uint32_t)(q4 * 32) << 16;
+    const bool issuer = (tid == 0);
     const int64_t soff = ((int64_t)ch.seq * H + h) * D * D;
-    bool ok = true;
+    bool bad = false;
     if (nchunks > 0) {
-      // initial state: bf16 copy and fp32 scaled by e^{G_C} of chunk 0
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars[B_GATE + 0], 0, abort, kWaitNs));
-      const float* eg0 = (const float*)(sm + SM_EGC);
+      // --- initial state: bf16 copy and fp32 scaled by e^{G_C} of chunk 0
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_GATE + 0], 0, abort, kWaitNs))) bad = true;
+      if (!bad) {
+        const float* eg0 = (const float*)(sm + SM_EGC);
 #pragma unroll 1
-      for (int blk = 0; blk < 4 && ok; ++blk) {
-        uint32_t f[32], b[16];
+        for (int blk = 0; blk < 4; ++blk) {
+          uint32_t f[32], b[16];
 #pragma unroll
-        for (int p = 0; p < 16; ++p) {
-          const int i0 = 32 * blk + 2 * p;
-          const float s0 = args.init_state ? args.init_state[soff + (int64_t)i0 * D + dv] : 0.0f;
-          const float s1 = args.init_state ? args.init_state[soff + (int64_t)(i0 + 1) * D + dv] : 0.0f;
-          b[p] = pack_bf16x2(s0, s1);
-          f[2 * p] = __float_as_uint(s0 * eg0[i0]);
-          f[2 * p + 1] = __float_as_uint(s1 * eg0[i0 + 1]);
+          for (int p = 0; p < 16; ++p) {
+            const int i0 = 32 * blk + 2 * p;
+            const float s0 = args.init_state ? args.init_state[soff + (int64_t)i0 * D + dv] : 0.0f;
+            const float s1 =
+                args.init_state ? args.init_state[soff + (int64_t)(i0 + 1) * D + dv] : 0.0f;
+            b[p] = pack_bf16x2(s0, s1);
+            f[2 * p] = __float_as_uint(s0 * eg0[i0]);
+            f[2 * p + 1] = __float_as_uint(s1 * eg0[i0 + 1]);
+          }
+          tmem_st_x16(tmem + lb + TM_SBF + 16 * blk, b);
+          tmem_st_x32(tmem + lb + TM_S + 32 * blk, f);
         }
-        tmem_st_x16(tmem + lb + TM_SBF + 16 * blk, b);
-        tmem_st_x32(tmem + lb + TM_S + 32 * blk, f);
+        tmem_wait_st();
       }
-      tmem_wait_st();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_STATE]);
-      for (int n = 0; n < nchunks && ok; ++n) {
-        const int buf = n & 1;
-        const uint32_t uo = tmem + lb + TM_UO + 32 * buf;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_UREADY], n & 1, abort, kWaitNs))) {
-          ok = false;
-          break;
+
+      // issue the [U' | 0] and [U | O] products of chunk m into buffer m & 1
+      auto issue_x = [&](int m) -> bool {
+        const int slot = m % NSLOT, b = m & 1, cc = m & 3, g = m >> 2;
+        if (!mbar_wait(&bars[B_CHUNK + slot], (m / NSLOT) & 1, abort, kWaitNs)) return false;
+        KTRACE(m, 10);
+        tc_fence_after();
+        const uint32_t ua = tmem + TM_UA + 32 * b, ub = tmem + TM_UB + 32 * b;
+        mma_ts(ua, tmem + TM_VT + 8 * slot, sdesc_noswz(sbase + SM_TB + slot * 1024, 512, 128),
+               idesc_bf16_f32(128, 32), 0);
+        const uint32_t ga = sbase + SM_GA + (g & 1) * GA_BYTES + cc * 32 * 128;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          // accumulator A: K = 0..63 (k-atom 0); accumulator B: K = 64..127 (k-atom 1)
+          mma_ts(ua, tmem + TM_SBF + 8 * kk, sdesc_sw128(ga + kk * 32), idesc_bf16_f32(128, 32), 1);
+          mma_ts(ub, tmem + TM_SBF + 8 * (kk + 4), sdesc_sw128(ga + 128 * 128 + kk * 32),
+                 idesc_bf16_f32(128, 32), kk > 0);
         }
-        if (lane == 0 && q4 == 2) KTRACE(n, 10);
+        mma_commit(&bars[B_X]);
+        return true;
+      };
+
+      if (bar_sync_or(NB_STATE, 128, bad || *abort)) bad = true;
+      if (!bad && issuer && !issue_x(0)) fail(abort, args.status);
+
+      float Uc[16], Dc[16];  // U and q.k of the current chunk (fp32), kept for its outputs
+      float Dn[16];          // q.k of the next chunk
+      {
+        const float* dp = (const float*)(sm + SM_DIAG);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          Dc[t] = dp[t] + dp[C + t] + dp[2 * C + t] + dp[3 * C + t];
+          Dn[t] = 0.0f;
+        }
+      }
+      for (int n = 0; n < nchunks && !bad; ++n) {
+        const int b = n & 1;
+        const uint32_t ua = tmem + lb + TM_UA + 32 * b, ub = tmem + lb + TM_UB + 32 * b;
+        // ---- U = U' - W S (two partial accumulators), as bf16 high/low for the products
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_X], n & 1, abort, kWaitNs))) bad = true;
+        if (issuer) KTRACE(n, 5);
         tc_fence_after();
         {
-          // U^T as bf16 high part (columns 0..7) and low part (columns 8..15)
-          uint32_t u[16], w[16];
-          tmem_ld_x16(uo, u);
+          uint32_t ra[16], rb[16], w[16];
+          tmem_ld_x16(ua, ra);
+          tmem_ld_x16(ub, rb);
           tmem_wait_ld();
 #pragma unroll
           for (int p = 0; p < 8; ++p) {
-            const float x0 = __uint_as_float(u[2 * p]), x1 = __uint_as_float(u[2 * p + 1]);
+            const float x0 = __uint_as_float(ra[2 * p]) + __uint_as_float(rb[2 * p]);
+            const float x1 = __uint_as_float(ra[2 * p + 1]) + __uint_as_float(rb[2 * p + 1]);
+            Uc[2 * p] = x0;
+            Uc[2 * p + 1] = x1;
             w[p] = pack_bf16x2(x0, x1);
             const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&w[p]);
             w[8 + p] = pack_bf16x2(x0 - __low2float(hb), x1 - __high2float(hb));
@@ -575,73 +604,113 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
         }
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[B_UBF]);
-        if (lane == 0 && q4 == 2) KTRACE(n, 11);
-        __syncwarp();
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_SODONE], n & 1, abort, kWaitNs))) {
-          ok = false;
+        if (bar_sync_or(NB_STATE, 128, bad || *abort)) {
+          bad = true;
           break;
         }
-        if (lane == 0 && q4 == 2) KTRACE(n, 12);
+        if (issuer) {
+          KTRACE(n, 6);
+          tc_fence_after();
+          const int slot = n % NSLOT;
+          const uint64_t kc = sdesc_noswz(sbase + SM_KC + slot * TILE, 2048, 128);
+          const uint64_t pp = sdesc_noswz(sbase + SM_P + slot * 512, 256, 128);
+          mma_ts(tmem + TM_S, tmem + TM_UBF, kc, idesc_bf16_f32(128, 128), 1);
+          mma_ts(tmem + TM_UA + 32 * b + 16, tmem + TM_UBF, pp, idesc_bf16_f32(128, 16), 1);
+          mma_ts(tmem + TM_S, tmem + TM_UBF + 8, kc, idesc_bf16_f32(128, 128), 1);
+          mma_ts(tmem + TM_UA + 32 * b + 16, tmem + TM_UBF + 8, pp, idesc_bf16_f32(128, 16), 1);
+          mma_commit(&bars[B_SO]);
+          if ((n & 3) == 3 || n == nchunks - 1) mma_commit(&bars[B_GFREE + ((n >> 2) & 1)]);
+        }
+        // ---- wait for the state product, then the state pass
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_SO], n & 1, abort, kWaitNs))) {
+          bad = true;
+          break;
+        }
+        if (issuer) KTRACE(n, 7);
         tc_fence_after();
         if (n + 1 < nchunks) {
           const int nslot = (n + 1) % NSLOT;
           if (!__all_sync(0xffffffffu,
                           mbar_wait(&bars[B_GATE + nslot], ((n + 1) / NSLOT) & 1, abort, kWaitNs))) {
-            ok = false;
+            bad = true;
             break;
           }
-          const float* eg = (const float*)(sm + SM_EGC + nslot * D * 4);
-#pragma unroll 1
+          uint32_t f[128];
+          tmem_ld_x32(tmem + lb + TM_S + 0, *reinterpret_cast<uint32_t(*)[32]>(&f[0]));
+          tmem_ld_x32(tmem + lb + TM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&f[32]));
+          tmem_ld_x32(tmem + lb + TM_S + 64, *reinterpret_cast<uint32_t(*)[32]>(&f[64]));
+          tmem_ld_x32(tmem + lb + TM_S + 96, *reinterpret_cast<uint32_t(*)[32]>(&f[96]));
+          tmem_wait_ld();
+#pragma unroll
           for (int blk = 0; blk < 4; ++blk) {
-            uint32_t f[32], b[16];
-            tmem_ld_x32(tmem + lb + TM_S + 32 * blk, f);
-            tmem_wait_ld();
+            uint32_t bf[16];
 #pragma unroll
             for (int p = 0; p < 16; ++p)
-              b[p] = pack_bf16x2(__uint_as_float(f[2 * p]), __uint_as_float(f[2 * p + 1]));
-            tmem_st_x16(tmem + lb + TM_SBF + 16 * blk, b);
-            const float4* eg4 = (const float4*)(eg + 32 * blk);
-#pragma unroll
-            for (int i4 = 0; i4 < 8; ++i4) {
-              const float4 e = eg4[i4];
-              f[4 * i4 + 0] = __float_as_uint(__uint_as_float(f[4 * i4 + 0]) * e.x);
-              f[4 * i4 + 1] = __float_as_uint(__uint_as_float(f[4 * i4 + 1]) * e.y);
-              f[4 * i4 + 2] = __float_as_uint(__uint_as_float(f[4 * i4 + 2]) * e.z);
-              f[4 * i4 + 3] = __float_as_uint(__uint_as_float(f[4 * i4 + 3]) * e.w);
-            }
-            tmem_st_x32(tmem + lb + TM_S + 32 * blk, f);
+              bf[p] = pack_bf16x2(__uint_as_float(f[32 * blk + 2 * p]),
+                                  __uint_as_float(f[32 * blk + 2 * p + 1]));
+            tmem_st_x16(tmem + lb + TM_SBF + 16 * blk, bf);
           }
           tmem_wait_st();
           tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[B_STATE]);
-          if (lane == 0 && q4 == 2) KTRACE(n, 13);
-          __syncwarp();
+          if (bar_sync_or(NB_STATE, 128, bad || *abort)) {
+            bad = true;
+            break;
+          }
+          if (issuer) {
+            KTRACE(n, 8);
+            if (!issue_x(n + 1)) fail(abort, args.status);
+          }
+          // fp32 state scaled by e^{G_C} of chunk n+1 (read by its state product)
+          const float4* eg4 = (const float4*)(sm + SM_EGC + nslot * D * 4);
+#pragma unroll
+          for (int i4 = 0; i4 < 32; ++i4) {
+            const float4 e = eg4[i4];
+            f[4 * i4 + 0] = __float_as_uint(__uint_as_float(f[4 * i4 + 0]) * e.x);
+            f[4 * i4 + 1] = __float_as_uint(__uint_as_float(f[4 * i4 + 1]) * e.y);
+            f[4 * i4 + 2] = __float_as_uint(__uint_as_float(f[4 * i4 + 2]) * e.z);
+            f[4 * i4 + 3] = __float_as_uint(__uint_as_float(f[4 * i4 + 3]) * e.w);
+          }
+          tmem_st_x32(tmem + lb + TM_S + 0, *reinterpret_cast<uint32_t(*)[32]>(&f[0]));
+          tmem_st_x32(tmem + lb + TM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&f[32]));
+          tmem_st_x32(tmem + lb + TM_S + 64, *reinterpret_cast<uint32_t(*)[32]>(&f[64]));
+          tmem_st_x32(tmem + lb + TM_S + 96, *reinterpret_cast<uint32_t(*)[32]>(&f[96]));
+          tmem_wait_st();
+          tc_fence_before();
+          if (issuer) KTRACE(n, 9);
+          // q.k diagonals of chunk n+1
+          const float* dp = (const float*)(sm + SM_DIAG + nslot * 4 * C * 4);
+#pragma unroll
+          for (int t = 0; t < 16; ++t) Dn[t] = dp[t] + dp[C + t] + dp[2 * C + t] + dp[3 * C + t];
         }
-        // output rows of this chunk
+        // ---- outputs of chunk n: O = [Qt S]_A + [Qt S]_B + P U + (q.k) U
         {
-          uint32_t o[16];
-          tmem_ld_x16(uo + 16, o);
+          uint32_t oa[16], ob[16];
+          tmem_ld_x16(ua + 16, oa);
+          tmem_ld_x16(ub + 16, ob);
           tmem_wait_ld();
           const int nvalid = min(C, L - n * C);
-          if (lane == 0 && q4 == 2) KTRACE(n, 14);
           const int64_t row0 = ch.t0 + (int64_t)n * C;
           if (args.out_bf16) {
             __nv_bfloat16* out = (__nv_bfloat16*)args.out;
 #pragma unroll
             for (int i = 0; i < C; ++i)
-              if (i < nvalid) out[((row0 + i) * H + h) * D + dv] = __float2bfloat16_rn(__uint_as_float(o[i]));
+              if (i < nvalid)
+                out[((row0 + i) * H + h) * D + dv] = __float2bfloat16_rn(
+                    __uint_as_float(oa[i]) + __uint_as_float(ob[i]) + Dc[i] * Uc[i]);
           } else {
             float* out = (float*)args.out;
 #pragma unroll
             for (int i = 0; i < C; ++i)
-              if (i < nvalid) out[((row0 + i) * H + h) * D + dv] = __uint_as_float(o[i]);
+              if (i < nvalid)
+                out[((row0 + i) * H + h) * D + dv] =
+                    __uint_as_float(oa[i]) + __uint_as_float(ob[i]) + Dc[i] * Uc[i];
           }
+          if (issuer) KTRACE(n, 12);
         }
+#pragma unroll
+        for (int t = 0; t < 16; ++t) Dc[t] = Dn[t];
       }
-      if (ok && args.final_state) {
+      if (!bad && args.final_state) {
 #pragma unroll 1
         for (int blk = 0; blk < 4; ++blk) {
           uint32_t f[32];
@@ -652,7 +721,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             args.final_state[soff + (int64_t)(32 * blk + i) * D + dv] = __uint_as_float(f[i]);
         }
       }
-      if (!ok) fail(abort, args.status);
+      if (bad) fail(abort, args.status);
+      if (issuer) {
+        mma_commit(&bars[B_DRAIN]);
+        mbar_wait_drain(&bars[B_DRAIN], 0, kWaitNs);
+      }
     } else if (args.final_state) {
       // empty sequence: the final state is the initial state
       for (int i = 0; i < D; ++i)
