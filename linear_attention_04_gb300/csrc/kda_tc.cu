@@ -77,7 +77,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
 
 // tensor memory columns (512 allocated)
-constexpr uint32_t TM_S = 0;      // fp32 S^T, 128 columns
+constexpr uint32_t TM_S = 0;      // fp32 dS^T = (KhC^T U)^T of a chunk, 128 columns
 constexpr uint32_t TM_SBF = 128;  // bf16 S^T (A operand), 64 columns
 constexpr uint32_t TM_AP = 192;   // A/P tiles of a group of 4 chunks, 64 columns
 constexpr uint32_t TM_UA = 256;   // [U | O] accumulator A (K = 0..63), 2 buffers x 32
@@ -248,9 +248,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = 4 * g + cc;
         if (n >= nchunks) break;
         const int s = n % NS, slot = n % NSLOT;
+        const int nvalid = min(C, L - n * C);
+        // beta of this chunk: the global load is issued first so that its
+        // latency hides behind the rest of phase A
+        unsigned short beta_r = 0;
+        if (it < nvalid)
+          beta_r = reinterpret_cast<const unsigned short*>(args.beta)[(ch.t0 + (int64_t)n * C + it) * H + h];
         if (!bad && !mbar_wait(&bars[B_FULL + s], (n / NS) & 1, abort, kWaitNs)) bad = true;
         if (it == 0) KTRACE(n, 1);
-        const int nvalid = min(C, L - n * C);
         const unsigned char* st = sm + SM_RING + s * 4 * TILE;
         const uint32_t* sq = (const uint32_t*)(st + 0 * TILE);
         const uint32_t* sk = (const uint32_t*)(st + 1 * TILE);
@@ -343,12 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ((float*)(sm + SM_DIAG + slot * 4 * C * 4))[wq * C + row] = v1;
           }
         }
-        if (it < C) {
-          const float b = it < nvalid
-                              ? __bfloat162float(args.beta[(ch.t0 + (int64_t)n * C + it) * H + h])
-                              : 0.0f;
-          ((float*)(sm + SM_BETA + slot * C * 4))[it] = b;
-        }
+        if (it < C) ((unsigned short*)(sm + SM_BETA + slot * C * 4))[it] = beta_r;
         {
           // V^T into tensor memory: TMEM lane = value channel 32*q4 + lane.  This
           // thread holds channels {lane & ~1, lane | 1} (of this warp's 32) for
@@ -416,12 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_x16(tmem + ((uint32_t)(q4 * 32) << 16) + TM_AP + 16 * q4, raw);
         tmem_wait_ld();
         float* Ab = (float*)(sm + SM_ABUF) + q4 * (C * 17);
-        const float* bet = (const float*)(sm + SM_BETA + slot * C * 4);
+        const __nv_bfloat16* bet = (const __nv_bfloat16*)(sm + SM_BETA + slot * C * 4);
         unsigned char* Pt = sm + SM_P + slot * 512;
         unsigned char* Tb = sm + SM_TB + slot * 1024;
         if (lane < 16) {
           const int i = lane;
-          const float bi = bet[i];
+          const float bi = __bfloat162float(bet[i]);
 #pragma unroll
           for (int j = 0; j < C; ++j) Ab[i * 17 + j] = (j < i) ? bi * __uint_as_float(raw[j]) : 0.0f;
         } else {
@@ -445,12 +445,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < C; ++i) t[i] = (i == j) ? 1.0f : 0.0f;
 #pragma unroll
           for (int i = 1; i < C; ++i) {
-            float acc = 0.0f;
+            float acc0 = 0.0f, acc1 = 0.0f;  // two partial sums: shorter dependency chain
 #pragma unroll
-            for (int m = 0; m < i; ++m) acc += Ab[i * 17 + m] * t[m];
-            if (i > j) t[i] = -acc;
+            for (int m = 0; m < i; m += 2) {
+              acc0 = fmaf(Ab[i * 17 + m], t[m], acc0);
+              if (m + 1 < i) acc1 = fmaf(Ab[i * 17 + m + 1], t[m + 1], acc1);
+            }
+            if (i > j) t[i] = -(acc0 + acc1);
           }
-          const float bj = bet[j];
+          const float bj = __bfloat162float(bet[j]);
 #pragma unroll
           for (int i = 0; i < C; ++i)
             *(__nv_bfloat16*)(Tb + (i & 7) * 16 + (i >> 3) * 128 + (j >> 3) * 512 + (j & 7) * 2) =
@@ -520,28 +523,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t soff = ((int64_t)ch.seq * H + h) * D * D;
     bool bad = false;
     if (nchunks > 0) {
-      // --- initial state: bf16 copy and fp32 scaled by e^{G_C} of chunk 0
+      // The fp32 state row of this thread (value channel dv, key channels 0..127)
+      // lives in registers; TMEM holds its bf16 copy (the A operand of the
+      // state products) and receives dS = U^T KhC from the tensor core.
+      float S[D];
       if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_GATE + 0], 0, abort, kWaitNs))) bad = true;
-      if (!bad) {
-        const float* eg0 = (const float*)(sm + SM_EGC);
-#pragma unroll 1
-        for (int blk = 0; blk < 4; ++blk) {
-          uint32_t f[32], b[16];
 #pragma unroll
-          for (int p = 0; p < 16; ++p) {
-            const int i0 = 32 * blk + 2 * p;
-            const float s0 = args.init_state ? args.init_state[soff + (int64_t)i0 * D + dv] : 0.0f;
-            const float s1 =
-                args.init_state ? args.init_state[soff + (int64_t)(i0 + 1) * D + dv] : 0.0f;
-            b[p] = pack_bf16x2(s0, s1);
-            f[2 * p] = __float_as_uint(s0 * eg0[i0]);
-            f[2 * p + 1] = __float_as_uint(s1 * eg0[i0 + 1]);
-          }
-          tmem_st_x16(tmem + lb + TM_SBF + 16 * blk, b);
-          tmem_st_x32(tmem + lb + TM_S + 32 * blk, f);
-        }
-        tmem_wait_st();
+      for (int i = 0; i < D; ++i)
+        S[i] = args.init_state ? args.init_state[soff + (int64_t)i * D + dv] : 0.0f;
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        uint32_t b16[16];
+#pragma unroll
+        for (int p = 0; p < 16; ++p) b16[p] = pack_bf16x2(S[32 * blk + 2 * p], S[32 * blk + 2 * p + 1]);
+        tmem_st_x16(tmem + lb + TM_SBF + 16 * blk, b16);
       }
+      tmem_wait_st();
       tc_fence_before();
 
       // issue the [U' | 0] and [U | O] products of chunk m into buffer m & 1
@@ -568,18 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (bar_sync_or(NB_STATE, 128, bad || *abort)) bad = true;
       if (!bad && issuer && !issue_x(0)) fail(abort, args.status);
 
-      float Uc[16], Dc[16];  // U and q.k of the current chunk (fp32), kept for its outputs
-      float Dn[16];          // q.k of the next chunk
-      {
-        const float* dp = (const float*)(sm + SM_DIAG);
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          Dc[t] = dp[t] + dp[C + t] + dp[2 * C + t] + dp[3 * C + t];
-          Dn[t] = 0.0f;
-        }
-      }
       for (int n = 0; n < nchunks && !bad; ++n) {
-        const int b = n & 1;
+        const int b = n & 1, slot = n % NSLOT;
         const uint32_t ua = tmem + lb + TM_UA + 32 * b, ub = tmem + lb + TM_UB + 32 * b;
         // ---- U = U' - W S (two partial accumulators), as bf16 high/low for the products
         if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_X], n & 1, abort, kWaitNs))) bad = true;
@@ -594,8 +581,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int p = 0; p < 8; ++p) {
             const float x0 = __uint_as_float(ra[2 * p]) + __uint_as_float(rb[2 * p]);
             const float x1 = __uint_as_float(ra[2 * p + 1]) + __uint_as_float(rb[2 * p + 1]);
-            Uc[2 * p] = x0;
-            Uc[2 * p + 1] = x1;
             w[p] = pack_bf16x2(x0, x1);
             const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&w[p]);
             w[8 + p] = pack_bf16x2(x0 - __low2float(hb), x1 - __high2float(hb));
@@ -611,45 +596,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (issuer) {
           KTRACE(n, 6);
           tc_fence_after();
-          const int slot = n % NSLOT;
           const uint64_t kc = sdesc_noswz(sbase + SM_KC + slot * TILE, 2048, 128);
           const uint64_t pp = sdesc_noswz(sbase + SM_P + slot * 512, 256, 128);
-          mma_ts(tmem + TM_S, tmem + TM_UBF, kc, idesc_bf16_f32(128, 128), 1);
+          mma_ts(tmem + TM_S, tmem + TM_UBF, kc, idesc_bf16_f32(128, 128), 0);
           mma_ts(tmem + TM_UA + 32 * b + 16, tmem + TM_UBF, pp, idesc_bf16_f32(128, 16), 1);
           mma_ts(tmem + TM_S, tmem + TM_UBF + 8, kc, idesc_bf16_f32(128, 128), 1);
           mma_ts(tmem + TM_UA + 32 * b + 16, tmem + TM_UBF + 8, pp, idesc_bf16_f32(128, 16), 1);
           mma_commit(&bars[B_SO]);
-          if ((n & 3) == 3 || n == nchunks - 1) mma_commit(&bars[B_GFREE + ((n >> 2) & 1)]);
         }
-        // ---- wait for the state product, then the state pass
+        // e^{G_C} of this chunk; its slot is recycled only after the group's
+        // release, which follows this chunk's outputs
+        const float4* eg = (const float4*)(sm + SM_EGC + slot * D * 4);
+        // ---- wait for dS = U^T KhC, then S <- e^{G_C} S + dS and its bf16 copy
         if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_SO], n & 1, abort, kWaitNs))) {
           bad = true;
           break;
         }
         if (issuer) KTRACE(n, 7);
         tc_fence_after();
-        if (n + 1 < nchunks) {
-          const int nslot = (n + 1) % NSLOT;
-          if (!__all_sync(0xffffffffu,
-                          mbar_wait(&bars[B_GATE + nslot], ((n + 1) / NSLOT) & 1, abort, kWaitNs))) {
-            bad = true;
-            break;
-          }
-          uint32_t f[128];
-          tmem_ld_x32(tmem + lb + TM_S + 0, *reinterpret_cast<uint32_t(*)[32]>(&f[0]));
-          tmem_ld_x32(tmem + lb + TM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&f[32]));
-          tmem_ld_x32(tmem + lb + TM_S + 64, *reinterpret_cast<uint32_t(*)[32]>(&f[64]));
-          tmem_ld_x32(tmem + lb + TM_S + 96, *reinterpret_cast<uint32_t(*)[32]>(&f[96]));
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t ds[64];
+          tmem_ld_x32(tmem + lb + TM_S + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&ds[0]));
+          tmem_ld_x32(tmem + lb + TM_S + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&ds[32]));
           tmem_wait_ld();
 #pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
-            uint32_t bf[16];
-#pragma unroll
-            for (int p = 0; p < 16; ++p)
-              bf[p] = pack_bf16x2(__uint_as_float(f[32 * blk + 2 * p]),
-                                  __uint_as_float(f[32 * blk + 2 * p + 1]));
-            tmem_st_x16(tmem + lb + TM_SBF + 16 * blk, bf);
+          for (int i4 = 0; i4 < 16; ++i4) {
+            const float4 e = eg[16 * half + i4];  // shared-memory broadcast
+            const int i = 64 * half + 4 * i4;
+            S[i + 0] = fmaf(S[i + 0], e.x, __uint_as_float(ds[4 * i4 + 0]));
+            S[i + 1] = fmaf(S[i + 1], e.y, __uint_as_float(ds[4 * i4 + 1]));
+            S[i + 2] = fmaf(S[i + 2], e.z, __uint_as_float(ds[4 * i4 + 2]));
+            S[i + 3] = fmaf(S[i + 3], e.w, __uint_as_float(ds[4 * i4 + 3]));
           }
+          if (n + 1 < nchunks) {
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+              uint32_t b16[16];
+              const int i0 = 64 * half + 32 * blk;
+#pragma unroll
+              for (int p = 0; p < 16; ++p) b16[p] = pack_bf16x2(S[i0 + 2 * p], S[i0 + 2 * p + 1]);
+              tmem_st_x16(tmem + lb + TM_SBF + 32 * half + 16 * blk, b16);
+            }
+          }
+        }
+        if (n + 1 < nchunks) {
           tmem_wait_st();
           tc_fence_before();
           if (bar_sync_or(NB_STATE, 128, bad || *abort)) {
@@ -658,36 +649,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (issuer) {
             KTRACE(n, 8);
+            // the previous group's slots may be recycled: its outputs are done
+            if ((n & 3) == 0 && n > 0) mma_commit(&bars[B_GFREE + (((n >> 2) - 1) & 1)]);
             if (!issue_x(n + 1)) fail(abort, args.status);
           }
-          // fp32 state scaled by e^{G_C} of chunk n+1 (read by its state product)
-          const float4* eg4 = (const float4*)(sm + SM_EGC + nslot * D * 4);
-#pragma unroll
-          for (int i4 = 0; i4 < 32; ++i4) {
-            const float4 e = eg4[i4];
-            f[4 * i4 + 0] = __float_as_uint(__uint_as_float(f[4 * i4 + 0]) * e.x);
-            f[4 * i4 + 1] = __float_as_uint(__uint_as_float(f[4 * i4 + 1]) * e.y);
-            f[4 * i4 + 2] = __float_as_uint(__uint_as_float(f[4 * i4 + 2]) * e.z);
-            f[4 * i4 + 3] = __float_as_uint(__uint_as_float(f[4 * i4 + 3]) * e.w);
-          }
-          tmem_st_x32(tmem + lb + TM_S + 0, *reinterpret_cast<uint32_t(*)[32]>(&f[0]));
-          tmem_st_x32(tmem + lb + TM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&f[32]));
-          tmem_st_x32(tmem + lb + TM_S + 64, *reinterpret_cast<uint32_t(*)[32]>(&f[64]));
-          tmem_st_x32(tmem + lb + TM_S + 96, *reinterpret_cast<uint32_t(*)[32]>(&f[96]));
-          tmem_wait_st();
-          tc_fence_before();
-          if (issuer) KTRACE(n, 9);
-          // q.k diagonals of chunk n+1
-          const float* dp = (const float*)(sm + SM_DIAG + nslot * 4 * C * 4);
-#pragma unroll
-          for (int t = 0; t < 16; ++t) Dn[t] = dp[t] + dp[C + t] + dp[2 * C + t] + dp[3 * C + t];
         }
-        // ---- outputs of chunk n: O = [Qt S]_A + [Qt S]_B + P U + (q.k) U
+        // ---- outputs of chunk n: O = [Qt S]_A + [Qt S]_B + P U + (q.k) U, with U
+        // re-read from its accumulators and q.k from the intra group's partial sums
         {
-          uint32_t oa[16], ob[16];
+          uint32_t oa[16], ob[16], ra[16], rb[16];
           tmem_ld_x16(ua + 16, oa);
           tmem_ld_x16(ub + 16, ob);
+          tmem_ld_x16(ua, ra);
+          tmem_ld_x16(ub, rb);
+          const float4* dp4 = (const float4*)(sm + SM_DIAG + slot * 4 * C * 4);
+          float Dc[16];
+#pragma unroll
+          for (int t4 = 0; t4 < 4; ++t4) {
+            const float4 a0 = dp4[t4], a1 = dp4[4 + t4], a2 = dp4[8 + t4], a3 = dp4[12 + t4];
+            Dc[4 * t4 + 0] = (a0.x + a1.x) + (a2.x + a3.x);
+            Dc[4 * t4 + 1] = (a0.y + a1.y) + (a2.y + a3.y);
+            Dc[4 * t4 + 2] = (a0.z + a1.z) + (a2.z + a3.z);
+            Dc[4 * t4 + 3] = (a0.w + a1.w) + (a2.w + a3.w);
+          }
           tmem_wait_ld();
+          float Uc[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t) Uc[t] = __uint_as_float(ra[t]) + __uint_as_float(rb[t]);
           const int nvalid = min(C, L - n * C);
           const int64_t row0 = ch.t0 + (int64_t)n * C;
           if (args.out_bf16) {
@@ -707,19 +695,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (issuer) KTRACE(n, 12);
         }
-#pragma unroll
-        for (int t = 0; t < 16; ++t) Dc[t] = Dn[t];
       }
+      if (issuer) mma_commit(&bars[B_GFREE + (((nchunks - 1) >> 2) & 1)]);
       if (!bad && args.final_state) {
-#pragma unroll 1
-        for (int blk = 0; blk < 4; ++blk) {
-          uint32_t f[32];
-          tmem_ld_x32(tmem + lb + TM_S + 32 * blk, f);
-          tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            args.final_state[soff + (int64_t)(32 * blk + i) * D + dv] = __uint_as_float(f[i]);
-        }
+        for (int i = 0; i < D; ++i) args.final_state[soff + (int64_t)i * D + dv] = S[i];
       }
       if (bad) fail(abort, args.status);
       if (issuer) {
