@@ -38,18 +38,31 @@ KDA_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// try_wait with a suspend-time hint: the thread is parked by the hardware until
+// the phase completes or about `hint_ns` have passed, instead of polling.
+KDA_DEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+constexpr uint32_t kSleepHintNs = 100000;  // 0.1 ms per parked try_wait
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit_ns` of wall-clock time or as soon as *abort is set; returns false then.
 KDA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
                        uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -58,9 +71,9 @@ KDA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort
 KDA_DEV bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
