@@ -99,8 +99,10 @@ constexpr uint32_t SM_P = SM_KC + NSLOT * TILE;          // NSLOT x [16 x 16] bf
 constexpr uint32_t SM_TB = SM_P + NSLOT * 512;           // NSLOT x [32 x 16] bf16
 constexpr uint32_t SM_EGC = SM_TB + NSLOT * 1024;        // NSLOT x 128 fp32
 constexpr uint32_t SM_BETA = SM_EGC + NSLOT * D * 4;     // NSLOT x 16 fp32
-constexpr uint32_t SM_DIAG = SM_BETA + NSLOT * C * 4;    // NSLOT x 4 warps x 16 fp32
-constexpr uint32_t SM_ABUF = SM_DIAG + NSLOT * 4 * C * 4;  // 4 warps x [16 x 17] fp32
+constexpr uint32_t SM_DIAG = SM_BETA + NSLOT * C * 4;    // NSLOT x 16 fp32 (q_t . k_t)
+constexpr uint32_t SM_DPART = SM_DIAG + NSLOT * C * 4;   // 4 warps x 16 fp32 partial sums
+constexpr uint32_t SM_XCH = SM_DPART + 4 * C * 4;        // 2 halves x 64 channel pairs x f32x2
+constexpr uint32_t SM_ABUF = SM_XCH + 2 * 64 * 8;        // 4 warps x [16 x 17] fp32
 constexpr uint32_t SM_BARS = SM_ABUF + 4 * C * 17 * 4;   // mbarriers
 constexpr int NBARS = 48;
 constexpr uint32_t SM_MISC = SM_BARS + NBARS * 8;        // tmem base, abort flag
@@ -210,12 +212,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int it = tid - 128;         // 0..127
     const int q4 = warp & 3;          // TMEM lane quarter of this warp
     const int wq = warp - 4;          // warp index inside the group
-    const int cp = it >> 1;           // channel pair: channels 2cp, 2cp+1
-    const int hf = it & 1;            // token half: rows 8hf .. 8hf+7
+    const int hf = wq >> 1;           // token half of this warp: rows 8hf .. 8hf+7
+    const int cp = 32 * (wq & 1) + lane;  // channel pair: channels 2cp, 2cp+1
     const f32x2 kC2 = f2(-kLog2e, -kLog2e);
     const f32x2 kC1 = f2(args.g_min * kLog2e, args.g_min * kLog2e);
     const f32x2 kOne = f2(1.0f, 1.0f);
     const f32x2 kZero = 0ull;
+    f32x2* xch = (f32x2*)(sm + SM_XCH);      // per-half cumulative-sum totals
+    float* dpart = (float*)(sm + SM_DPART);  // per-warp q.k partial sums of a chunk
     // TMA loads of chunk m into ring stage m % NS (issued by one lane)
     auto load_chunk = [&](int m) {
       const int s = m % NS;
@@ -242,7 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       unsigned char* GA = sm + SM_GA + gb * GA_BYTES;
       if (g >= 2 && !bad && !mbar_wait(&bars[B_GFREE + gb], ((g >> 1) - 1) & 1, abort, kWaitNs))
         bad = true;
-      // ---- phase A: gate, cumulative sum, decayed operands of the group's chunks
+      // ---- phase A: gate, cumulative sum, decayed operands of the group's chunks.
+      // Warps 0,1 of the group take tokens 0..7, warps 2,3 tokens 8..15; each
+      // warp covers 64 channels (a full 128-byte row span: conflict-free).
       bool stop = false;
       for (int cc = 0; cc < 4; ++cc) {
         const int n = 4 * g + cc;
@@ -260,9 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t* sq = (const uint32_t*)(st + 0 * TILE);
         const uint32_t* sk = (const uint32_t*)(st + 1 * TILE);
         const uint32_t* sth = (const uint32_t*)(st + 2 * TILE);
-        const uint32_t* sv = (const uint32_t*)(st + 3 * TILE);
+        const unsigned short* sv = (const unsigned short*)(st + 3 * TILE);
         f32x2 Gr[8], kr[8], qr[8];
-        uint32_t vw[8];
         f32x2 G2 = kZero;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -271,17 +276,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const f32x2 th = bf2_to_f2(sth[r * 64 + cp]);
           kr[i] = valid ? bf2_to_f2(sk[r * 64 + cp]) : kZero;
           qr[i] = valid ? bf2_to_f2(sq[r * 64 + cp]) : kZero;
-          vw[i] = valid ? sv[r * 64 + cp] : 0u;
           const f32x2 x = mul2(th, kC2);
           const f32x2 den = add2(f2(ex2_approx(f2lo(x)), ex2_approx(f2hi(x))), kOne);
           const f32x2 g2 = mul2(f2(rcp_approx(f2lo(den)), rcp_approx(f2hi(den))), kC1);
           G2 = add2(G2, valid ? g2 : kZero);  // log2-domain cumulative log-decay
           Gr[i] = G2;
         }
-        // the second token half adds the first half's total; both need the chunk total
-        const f32x2 other =
-            ((uint64_t)__shfl_xor_sync(0xffffffffu, (uint32_t)(G2 >> 32), 1) << 32) |
-            (uint64_t)__shfl_xor_sync(0xffffffffu, (uint32_t)G2, 1);
+        // exchange the half totals: the second half adds the first half's total,
+        // both need the chunk total
+        xch[hf * 64 + cp] = G2;
+        if (bar_sync_or(NB_INTRA, 128, bad || *abort)) {
+          stop = true;
+          break;
+        }
+        const f32x2 other = xch[(1 - hf) * 64 + cp];
         if (hf) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) Gr[i] = add2(Gr[i], other);
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const f32x2 GT = add2(G2, other);  // chunk total (same in both halves)
         const f32x2 eGC = f2(ex2_approx(f2lo(GT)), ex2_approx(f2hi(GT)));
         uint32_t kc0[4], kc1[4];
-        float dpart[8];
+        float dq[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int r = 8 * hf + i;
@@ -308,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             kc1[i >> 1] = __float_as_uint(f2hi(khc));
           }
           const f32x2 qk = mul2(qr[i], kr[i]);
-          dpart[i] = f2lo(qk) + f2hi(qk);
+          dq[i] = f2lo(qk) + f2hi(qk);
         }
         {
           // KhC^T tile: row = key channel, 16 tokens along K (no swizzle);
@@ -321,14 +329,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             *(float2*)(sm + SM_EGC + slot * D * 4 + c0 * 4) = make_float2(f2lo(eGC), f2hi(eGC));
         }
         {
-          // q_t . k_t over this warp's 32 channels: reduce 8 rows over the 16
-          // lanes of the same token half (lane bits 1..4), one row per lane
+          // q_t . k_t over this warp's 64 channels: reduce 8 rows over the 32
+          // lanes, one row per group of four lanes
           const int b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
           float v4[4], v2[2], v1;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const float send = b4 ? dpart[j] : dpart[j + 4];
-            const float keep = b4 ? dpart[j + 4] : dpart[j];
+            const float send = b4 ? dq[j] : dq[j + 4];
+            const float keep = b4 ? dq[j + 4] : dq[j];
             v4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
           }
 #pragma unroll
@@ -343,31 +351,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             v1 = keep + __shfl_xor_sync(0xffffffffu, send, 4);
           }
           v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
-          if ((lane & 2) == 0) {
-            const int row = 8 * hf + 4 * b4 + 2 * b3 + b2;
-            ((float*)(sm + SM_DIAG + slot * 4 * C * 4))[wq * C + row] = v1;
-          }
+          v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+          if ((lane & 3) == 0) dpart[wq * C + 8 * hf + 4 * b4 + 2 * b3 + b2] = v1;
         }
         if (it < C) ((unsigned short*)(sm + SM_BETA + slot * C * 4))[it] = beta_r;
         {
-          // V^T into tensor memory: TMEM lane = value channel 32*q4 + lane.  This
-          // thread holds channels {lane & ~1, lane | 1} (of this warp's 32) for
-          // 8 tokens; it swaps the partner's channel with the partner.
-          uint32_t mine[4], give[4];
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const uint32_t a = vw[2 * p], b = vw[2 * p + 1];  // tokens 2p, 2p+1 of this half
-            const uint32_t lo = __byte_perm(a, b, 0x5410);    // channel 2cp   of both tokens
-            const uint32_t hi = __byte_perm(a, b, 0x7632);    // channel 2cp+1 of both tokens
-            mine[p] = (lane & 1) ? hi : lo;
-            give[p] = (lane & 1) ? lo : hi;
-          }
+          // V^T into tensor memory: TMEM lane = value channel 32*q4 + lane,
+          // 16 tokens packed two per 32-bit column
+          const int dv = 32 * q4 + lane;
           uint32_t w[8];
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const uint32_t got = __shfl_xor_sync(0xffffffffu, give[p], 1);
-            w[4 * hf + p] = mine[p];
-            w[4 * (1 - hf) + p] = got;
+          for (int p = 0; p < 8; ++p) {
+            const uint32_t v0 = (2 * p < nvalid) ? (uint32_t)sv[(2 * p) * D + dv] : 0u;
+            const uint32_t v1 = (2 * p + 1 < nvalid) ? (uint32_t)sv[(2 * p + 1) * D + dv] : 0u;
+            w[p] = v0 | (v1 << 16);
           }
           __syncwarp();
           tmem_st_x8(tmem + ((uint32_t)(q4 * 32) << 16) + TM_VT + 8 * slot, w);
@@ -379,14 +376,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           stop = true;
           break;
         }
-        if (it == 0) {
-          mbar_arrive(&bars[B_GATE + slot]);
-          KTRACE(n, 2);
-          if (n + NS < nchunks) {
-            // the whole group has consumed stage s: refill it
-            fence_proxy_async_smem();
-            load_chunk(n + NS);
-            issued = n + NS + 1;
+        if (wq == 0) {
+          // q.k of each token: the two half-warps' partial sums
+          if (lane < C) {
+            const int w0 = 2 * (lane >> 3);
+            ((float*)(sm + SM_DIAG + slot * C * 4))[lane] = dpart[w0 * C + lane] + dpart[(w0 + 1) * C + lane];
+          }
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars[B_GATE + slot]);
+            KTRACE(n, 2);
+            if (n + NS < nchunks) {
+              // the whole group has consumed stage s: refill it
+              load_chunk(n + NS);
+              issued = n + NS + 1;
+            }
           }
         }
       }
@@ -652,6 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the previous group's slots may be recycled: its outputs are done
             if ((n & 3) == 0 && n > 0) mma_commit(&bars[B_GFREE + (((n >> 2) - 1) & 1)]);
             if (!issue_x(n + 1)) fail(abort, args.status);
+            KTRACE(n + 1, 13);
           }
         }
         // ---- outputs of chunk n: O = [Qt S]_A + [Qt S]_B + P U + (q.k) U, with U
@@ -662,15 +667,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_x16(ub + 16, ob);
           tmem_ld_x16(ua, ra);
           tmem_ld_x16(ub, rb);
-          const float4* dp4 = (const float4*)(sm + SM_DIAG + slot * 4 * C * 4);
+          const float4* dp4 = (const float4*)(sm + SM_DIAG + slot * C * 4);
           float Dc[16];
 #pragma unroll
           for (int t4 = 0; t4 < 4; ++t4) {
-            const float4 a0 = dp4[t4], a1 = dp4[4 + t4], a2 = dp4[8 + t4], a3 = dp4[12 + t4];
-            Dc[4 * t4 + 0] = (a0.x + a1.x) + (a2.x + a3.x);
-            Dc[4 * t4 + 1] = (a0.y + a1.y) + (a2.y + a3.y);
-            Dc[4 * t4 + 2] = (a0.z + a1.z) + (a2.z + a3.z);
-            Dc[4 * t4 + 3] = (a0.w + a1.w) + (a2.w + a3.w);
+            const float4 a0 = dp4[t4];
+            Dc[4 * t4 + 0] = a0.x;
+            Dc[4 * t4 + 1] = a0.y;
+            Dc[4 * t4 + 2] = a0.z;
+            Dc[4 * t4 + 3] = a0.w;
           }
           tmem_wait_ld();
           float Uc[16];
