@@ -111,7 +111,7 @@ def traffic_from_profiles(kernel: str, workload: str) -> tuple[int | None, str |
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms in the background; keeps timestamps."""
+    """nvidia-smi sampled every 50 ms in the background; keeps timestamps."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -127,7 +127,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", self.gpu_id],
+                 "-lms", "50", "-i", self.gpu_id],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -321,7 +321,7 @@ def run_ours(args, rank, world, local):
     alg = algorithmic_bytes(w, inp)
     flops = chunk_gemm_flops(w, inp)
     achieved = alg / avg_launch_s / 1e9
-    kname = "kda_fwd_tc_kernel" if path == "tc" else "kda_fwd_simt_kernel"
+    kname = {"tc": "kda_fwd_tc_kernel", "mma": "kda_fwd_mma_kernel"}.get(path, "kda_fwd_simt_kernel")
     traffic, traffic_src = traffic_from_profiles(kname, w.name)
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -439,11 +439,11 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="train_bf16")
-    ap.add_argument("--path", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--path", choices=["auto", "simt", "tc", "mma"], default="auto")
     ap.add_argument("--seed", type=int, default=20261204)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)

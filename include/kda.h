@@ -80,9 +80,10 @@ extern "C" {
 #define KDA_ERR_UNSUPPORTED_SHAPE (-7)  /* dk/dv outside {16,32,64,128} for this path    */
 
 /* kernel path selection for kda_chunk_fwd_ex */
-#define KDA_PATH_AUTO 0 /* tensor-core path for bf16 when available, else SIMT        */
+#define KDA_PATH_AUTO 0 /* KDA_PATH_MMA for bf16 with dk = dv = 128, else SIMT        */
 #define KDA_PATH_SIMT 1 /* fp32 CUDA-core path (any supported dtype/shape)             */
 #define KDA_PATH_TC 2   /* tcgen05/TMEM tensor-core path (bf16, dk = dv = 128)         */
+#define KDA_PATH_MMA 3  /* register-resident mma.sync path (bf16, dk = dv = 128)       */
 
 /* element types of q, k, v, theta, beta and out */
 #define KDA_DTYPE_BF16 0
@@ -119,8 +120,8 @@ KDA_API int kda_chunk_fwd_f32(const float* q, const float* k, const float* v, co
  * path chosen explicitly.  `dtype` (KDA_DTYPE_*) is the type of q, k, v,
  * theta and beta; `out_dtype` that of out (KDA_DTYPE_F32, or KDA_DTYPE_BF16
  * to halve the output bytes at the cost of bf16 rounding of o; fp32 inputs
- * require an fp32 out).  `path` is KDA_PATH_*; KDA_PATH_TC requires bf16
- * inputs and dk = dv = 128 (else KDA_ERR_UNSUPPORTED_SHAPE). */
+ * require an fp32 out).  `path` is KDA_PATH_*; KDA_PATH_TC and KDA_PATH_MMA
+ * require bf16 inputs and dk = dv = 128 (else KDA_ERR_UNSUPPORTED_SHAPE). */
 typedef struct kda_fwd_args {
   const void* q;
   const void* k;
@@ -147,7 +148,7 @@ KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* args, cudaStream_t stream);
 KDA_API int kda_device_status(int clear);
 
 /* The kernel path kda_chunk_fwd_ex would take for these arguments with
- * KDA_PATH_AUTO (KDA_PATH_TC or KDA_PATH_SIMT), or a negative KDA_ERR_*. */
+ * KDA_PATH_AUTO (KDA_PATH_MMA or KDA_PATH_SIMT), or a negative KDA_ERR_*. */
 KDA_API int kda_select_path(int dtype, int dk, int dv);
 
 /* Human-readable text for a status code (static storage, never NULL). */

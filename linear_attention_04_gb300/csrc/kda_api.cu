@@ -56,7 +56,8 @@ int validate(const kda_fwd_args* a) {
   if (a->dtype != KDA_DTYPE_BF16 && a->dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
   if (a->out_dtype != KDA_DTYPE_BF16 && a->out_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
   if (a->dtype == KDA_DTYPE_F32 && a->out_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
-  if (a->path != KDA_PATH_AUTO && a->path != KDA_PATH_SIMT && a->path != KDA_PATH_TC)
+  if (a->path != KDA_PATH_AUTO && a->path != KDA_PATH_SIMT && a->path != KDA_PATH_TC &&
+      a->path != KDA_PATH_MMA)
     return KDA_ERR_INVALID_ARG;
   if (!shape_ok(a->dk) || !shape_ok(a->dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
   // sizes must fit the 32-bit grid and 64-bit offsets used by the kernels
@@ -78,7 +79,7 @@ extern "C" {
 KDA_API int kda_select_path(int dtype, int dk, int dv) {
   if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
   if (!kda::shape_ok(dk) || !kda::shape_ok(dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
-  return kda::tc_supported(dtype, dk, dv) ? KDA_PATH_TC : KDA_PATH_SIMT;
+  return kda::mma_supported(dtype, dk, dv) ? KDA_PATH_MMA : KDA_PATH_SIMT;
 }
 
 KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* a, cudaStream_t stream) {
@@ -87,6 +88,8 @@ KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* a, cudaStream_t stream) {
   int path = a->path;
   if (path == KDA_PATH_AUTO) path = kda_select_path(a->dtype, a->dk, a->dv);
   if (path == KDA_PATH_TC && !kda::tc_supported(a->dtype, a->dk, a->dv))
+    return KDA_ERR_UNSUPPORTED_SHAPE;
+  if (path == KDA_PATH_MMA && !kda::mma_supported(a->dtype, a->dk, a->dv))
     return KDA_ERR_UNSUPPORTED_SHAPE;
   rc = kda::check_device();
   if (rc != KDA_OK) return rc;
@@ -122,6 +125,7 @@ KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* a, cudaStream_t stream) {
     return KDA_OK;
   }
   if (path == KDA_PATH_TC) return kda::launch_tc(p, stream);
+  if (path == KDA_PATH_MMA) return kda::launch_mma(p, stream);
   return kda::launch_simt(p, stream);
 }
 

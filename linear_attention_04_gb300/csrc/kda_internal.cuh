@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libkda.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -37,6 +38,13 @@ int* status_word_device_ptr();
 int launch_simt(const FwdParams& p, cudaStream_t stream);
 int launch_tc(const FwdParams& p, cudaStream_t stream);
 bool tc_supported(int dtype, int dk, int dv);
+int launch_mma(const FwdParams& p, cudaStream_t stream);
+bool mma_supported(int dtype, int dk, int dv);
+
+// TMA map over a [tokens][H][128] bf16 tensor whose boxes are one chunk of 16
+// tokens x 128 channels of one head (unswizzled, out-of-range rows read 0).
+// False if the driver's encoder is unavailable or rejects the arguments.
+bool encode_token_rows(CUtensorMap* m, const void* base, int H, int64_t tokens);
 
 // Rank-ordered chain lookup for packed variable-length batches: blockIdx.x = r * H + h
 // runs the r-th longest sequence first (longest-processing-time order).  For

@@ -1,0 +1,654 @@
+// kda_mma.cu -- register-resident tensor-core path of the KDA chunked forward
+// pass (bf16 q, k, v, theta, beta; dk = dv = 128; fp32 state; fp32 or bf16 out).
+//
+// The recurrence S_t = (I - b_t k_t k_t^T) Diag(e^{g_t}) S_{t-1} + b_t k_t v_t^T,
+// o_t = S_t^T q_t ("Kimi K3 Deep Dive", section "Core Innovation 1") acts on
+// every value channel (column of S) separately: column j of S depends only on
+// k, g, b and column j of V.  So the dv = 128 value channels are split over
+// four warps, 32 each, and each warp carries its 128 x 32 slice of S in fp32
+// registers through the whole sequence, with no exchange between warps.
+//
+// Per 16-token chunk n (G = inclusive in-chunk cumulative log-decay,
+// Kt = K e^{G}, Qt = Q e^{G}, Kh = K e^{-G}, KhC = K e^{G_C - G}; every factor
+// lies in [e^{-80}, e^{80}] for g >= g_min = -5, "Kimi K3 Deep Dive", section
+// "The Design"):
+//
+//   A  = strict_lower(Diag(b) Kt Kh^T)      P = strict_lower(Qt Kh^T)
+//   Tb = (I + A)^{-1} Diag(b)               W = Tb Kt
+//   U  = Tb V - W S                         O = Qt S + P U + Diag(q_t . k_t) U
+//   S <- Diag(e^{G_C}) S + KhC^T U
+//
+// Warp roles (256 threads, one warp of each role per SM sub-partition):
+//   warps 0..3  state warps: warp w owns value channels 32w .. 32w+31.  Per
+//               chunk, with S^T (value channel x key channel) as the A operand
+//               taken straight from the fp32 accumulator registers (bf16 pairs):
+//                 [U | O] = [V^T Tb^T | 0] + S^T [-W | Qt]^T      (K = 128)
+//                 O      += U^T P^T (U as a bf16 high/low pair) + (q.k) U
+//                 S^T    <- S^T Diag(e^{G_C}) + U^T KhC           (K = 16)
+//               then the warp writes its outputs and releases the chunk slot.
+//   warps 4..7  intra warps: warp 4+i runs chunks i, i+4, i+8, ...; each
+//               loads its chunk with TMA (q, k, theta, v into a private stage,
+//               refilled with its next chunk as soon as the stage is read),
+//               computes the gate g = g_min * sigmoid(theta), the cumulative
+//               sums and the decayed operands in fp32, the chunk products A, P
+//               and W = Tb Kt with mma.sync, the triangular inverse by forward
+//               substitution, and fills a chunk slot for the state warps.
+//
+// All products are mma.sync m16n8k16 (bf16 operands, fp32 accumulation).
+// The chain of dependent products per chunk is short (a few dozen
+// instructions per warp between hand-offs) and every operand of the state
+// products stays in registers, which is what the sequential recurrence needs:
+// its speed is set by the latency of each step, not by tensor throughput.
+//
+// The diagonal of Qt Kh^T is q_t . k_t exactly (the decay factors cancel), so
+// it is taken in fp32 from the bf16 inputs and applied to U in fp32.
+//
+// Every wait is bounded: a wait that runs out sets the CTA's abort flag and the
+// device status word (KDA_ERR_DEVICE_TIMEOUT); every role then leaves its loop
+// and the TMA loads still in flight are drained before the CTA exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "kda_device.cuh"
+#include "kda_internal.cuh"
+#include "kda_sm100.cuh"
+
+namespace kda {
+namespace {
+
+using namespace sm100;
+
+constexpr int C = kChunk;  // 16
+constexpr int D = 128;     // dk = dv
+constexpr int kStateWarps = 4;
+constexpr int kIntraWarps = 4;
+constexpr int kThreads = 32 * (kStateWarps + kIntraWarps);
+constexpr int NSLOT = 6;  // chunk slots between the intra and the state warps
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- shared memory
+constexpr uint32_t ROW = D * 2;       // 256 bytes: one 128-channel bf16 row
+constexpr uint32_t TILE = C * ROW;    // 4096: a 16 x 128 bf16 tile
+constexpr uint32_t STAGE = 4 * TILE;  // q, k, theta, v of one chunk (TMA, unswizzled)
+
+// chunk slot, written by one intra warp and read by the four state warps
+constexpr uint32_t SL_XB = 0;                 // [32][128] bf16: rows 0..15 Kt, then -W; 16..31 Qt
+constexpr uint32_t SL_KC = SL_XB + 2 * TILE;  // [16][128] bf16 KhC (token-major)
+constexpr uint32_t SL_V = SL_KC + TILE;       // [16][128] bf16 V (rows past the end zeroed)
+constexpr uint32_t SL_TB = SL_V + TILE;       // [16][16] bf16 Tb
+constexpr uint32_t SL_P = SL_TB + 512;        // [16][16] bf16 strictly lower P
+constexpr uint32_t SL_EGC = SL_P + 512;       // [128] fp32 e^{G_C}
+constexpr uint32_t SL_DC = SL_EGC + 512;      // [16] fp32 q_t . k_t
+constexpr uint32_t SLOT_BYTES = SL_DC + 128;
+
+constexpr uint32_t SM_RING = 0;                               // kIntraWarps x STAGE
+constexpr uint32_t SM_KH = SM_RING + kIntraWarps * STAGE;     // kIntraWarps x [16][128] bf16 Kh
+constexpr uint32_t SM_AB = SM_KH + kIntraWarps * TILE;        // kIntraWarps x [16][16] fp32 A
+constexpr uint32_t AB_BYTES = C * C * 4;
+constexpr uint32_t SM_SLOTS = SM_AB + kIntraWarps * AB_BYTES;
+constexpr uint32_t SM_BARS = SM_SLOTS + NSLOT * SLOT_BYTES;
+constexpr int B_FULL = 0;                     // [kIntraWarps] TMA -> intra warp
+constexpr int B_READY = kIntraWarps;          // [NSLOT] intra warp -> state warps
+constexpr int B_FREE = kIntraWarps + NSLOT;   // [NSLOT] state warps (4 arrivals) -> intra warp
+constexpr int NBARS = kIntraWarps + 2 * NSLOT;
+constexpr uint32_t SM_MISC = SM_BARS + NBARS * 8;  // abort flag
+constexpr uint32_t SM_RANK = SM_MISC + 16;         // chain-order scratch
+constexpr uint32_t SM_TOTAL = SM_RANK + (kMaxRankedSeqsDev + 1) * 4;
+constexpr uint32_t SMEM_BYTES = SM_TOTAL + 128;    // + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(SLOT_BYTES % 128 == 0 && SM_SLOTS % 128 == 0, "slot alignment");
+
+// Byte offset of (row, col) in a tile of 256-byte rows (128 bf16 channels)
+// whose 16-byte chunks are XOR-swizzled by row: eight consecutive rows of one
+// chunk column fall in distinct banks (conflict-free ldmatrix).
+__device__ __forceinline__ uint32_t sw256(int row, int col) {
+  const int c = col >> 3;
+  return (uint32_t)(row * 256 + (((c ^ row) & 7) | (c & 8)) * 16 + (col & 7) * 2);
+}
+// Same for 16 x 16 bf16 tiles (32-byte rows): chunk XOR (row / 4).
+__device__ __forceinline__ uint32_t sw32(int row, int col) {
+  return (uint32_t)(row * 32 + (((col >> 3) ^ (row >> 2)) & 1) * 16 + (col & 7) * 2);
+}
+
+// D += A B with mma.sync m16n8k16, bf16 operands, fp32 accumulators (a pure
+// register operation: not volatile, so the compiler may schedule it freely).
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+struct MmaArgs {
+  const __nv_bfloat16* beta;
+  float g_min;
+  const float* init_state;
+  void* out;
+  int out_bf16;
+  float* final_state;
+  const int32_t* cu_seqlens;
+  int N, H, T;
+  int* status;
+};
+
+// Optional event trace of the first CTA (compile with -DKDA_TRACE): wall-clock
+// time of each pipeline event per chunk, read back with kda_debug_trace_read_mma.
+constexpr int kTraceChunks = 512;
+#ifdef KDA_TRACE
+__device__ unsigned long long g_kda_trace_mma[kTraceChunks * 16];
+#define KTRACE(n, k)                                                                              \
+  do {                                                                                            \
+    if (blockIdx.x == 0 && (n) < kTraceChunks) g_kda_trace_mma[(n) * 16 + (k)] = globaltimer_ns(); \
+  } while (0)
+#define KTRACE_CLK(n, k)                                                               \
+  do {                                                                                 \
+    if (blockIdx.x == 0 && (n) < kTraceChunks) g_kda_trace_mma[(n) * 16 + (k)] = clock64(); \
+  } while (0)
+#else
+#define KTRACE(n, k) \
+  do {               \
+  } while (0)
+#define KTRACE_CLK(n, k) \
+  do {                   \
+  } while (0)
+#endif
+
+__device__ __forceinline__ void fail(volatile int* abort, int* status) {
+  *abort = 1;
+  atomicExch(status, KDA_ERR_DEVICE_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    kda_fwd_mma_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_th,
+                       const __grid_constant__ CUtensorMap tm_v, const MmaArgs args) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
+  uint64_t* bars = (uint64_t*)(sm + SM_BARS);
+  volatile int* abort = (volatile int*)(sm + SM_MISC);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // fragment coordinates of mma.sync (g: row group, q: column pair) and of
+  // ldmatrix.x4 (mi: which 8x8 matrix this lane addresses, rr: its row)
+  const int g = lane >> 2, q = lane & 3, mi = lane >> 3, rr = lane & 7;
+
+  const Chain ch = chain_for_block(blockIdx.x, args.H, args.N, args.T, args.cu_seqlens,
+                                   (int*)(sm + SM_RANK));
+  const int h = ch.head;
+  const int H = args.H;
+  const int L = (int)(ch.t1 - ch.t0);
+  const int nchunks = (L + C - 1) / C;
+
+  if (tid == 0) {
+    for (int i = 0; i < NBARS; ++i) mbar_init(&bars[i], (i >= B_FREE) ? kStateWarps : 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint32_t sbase = smem_u32(sm);
+
+  if (warp >= kStateWarps) {
+    // ================================================================ intra warps
+    const int iw = warp - kStateWarps;
+    unsigned char* st = sm + SM_RING + iw * STAGE;
+    const uint32_t khs = sbase + SM_KH + iw * TILE;
+    unsigned char* kh = sm + SM_KH + iw * TILE;
+    float* ab = (float*)(sm + SM_AB + iw * AB_BYTES);
+    uint64_t* full = &bars[B_FULL + iw];
+    auto load = [&](int m) {
+      mbar_arrive_expect_tx(full, STAGE);
+      const int row = (int)(ch.t0 + (int64_t)m * C);
+      tma_load_3d(st + 0 * TILE, &tm_q, 0, h, row, full);
+      tma_load_3d(st + 1 * TILE, &tm_k, 0, h, row, full);
+      tma_load_3d(st + 2 * TILE, &tm_th, 0, h, row, full);
+      tma_load_3d(st + 3 * TILE, &tm_v, 0, h, row, full);
+    };
+    int issued = 0, consumed = 0;
+    if (lane == 0 && iw < nchunks) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_th);
+      prefetch_tmap(&tm_v);
+      load(iw);
+    }
+    if (iw < nchunks) issued = 1;
+    bool bad = false;
+    const f32x2 kC2 = f2(-kLog2e, -kLog2e);
+    const f32x2 kC1 = f2(args.g_min * kLog2e, args.g_min * kLog2e);
+    const f32x2 kOne = f2(1.0f, 1.0f);
+    const f32x2 kZero = 0ull;
+    for (int n = iw; n < nchunks; n += kIntraWarps) {
+      const int slot = n % NSLOT;
+      const int nvalid = min(C, L - n * C);
+      unsigned char* sl = sm + SM_SLOTS + slot * SLOT_BYTES;
+      const uint32_t sls = sbase + SM_SLOTS + slot * SLOT_BYTES;
+      // beta of the chunk (lane t holds beta_t), issued before the waits
+      float beta_l = 0.0f;
+      if (lane < nvalid) beta_l = __bfloat162float(args.beta[(ch.t0 + (int64_t)n * C + lane) * H + h]);
+      if (!__all_sync(0xffffffffu, mbar_wait(full, consumed & 1, abort, kWaitNs))) {
+        bad = true;
+        break;
+      }
+      ++consumed;
+      if (lane == 0) KTRACE(n, 5);
+      if (n >= NSLOT &&
+          !__all_sync(0xffffffffu,
+                      mbar_wait(&bars[B_FREE + slot], ((n / NSLOT) - 1) & 1, abort, kWaitNs))) {
+        bad = true;
+        break;
+      }
+      if (lane == 0) KTRACE(n, 6);
+      // ---- phase A: gate, cumulative sums, decayed operands.  Lane l holds
+      // channels 4l .. 4l+3 of every token of the chunk.
+      const uint2* sq = (const uint2*)(st + 0 * TILE);
+      const uint2* sk = (const uint2*)(st + 1 * TILE);
+      const uint2* sth = (const uint2*)(st + 2 * TILE);
+      f32x2 G0 = kZero, G1 = kZero;  // log2-domain cumulative log-decay
+      f32x2 khr[C][2];               // Kh in fp32, for KhC once G_C is known
+      float dq[C];                   // partial q_t . k_t over this lane's channels
+#pragma unroll
+      for (int t = 0; t < C; ++t) {
+        const bool valid = t < nvalid;
+        const uint2 thw = sth[t * 32 + lane], kw = sk[t * 32 + lane], qw = sq[t * 32 + lane];
+        const f32x2 k0 = valid ? bf2_to_f2(kw.x) : kZero, k1 = valid ? bf2_to_f2(kw.y) : kZero;
+        const f32x2 q0 = valid ? bf2_to_f2(qw.x) : kZero, q1 = valid ? bf2_to_f2(qw.y) : kZero;
+        const f32x2 x0 = mul2(bf2_to_f2(thw.x), kC2), x1 = mul2(bf2_to_f2(thw.y), kC2);
+        const f32x2 d0 = add2(f2(ex2_approx(f2lo(x0)), ex2_approx(f2hi(x0))), kOne);
+        const f32x2 d1 = add2(f2(ex2_approx(f2lo(x1)), ex2_approx(f2hi(x1))), kOne);
+        const f32x2 g0 = mul2(f2(rcp_approx(f2lo(d0)), rcp_approx(f2hi(d0))), kC1);
+        const f32x2 g1 = mul2(f2(rcp_approx(f2lo(d1)), rcp_approx(f2hi(d1))), kC1);
+        G0 = add2(G0, valid ? g0 : kZero);
+        G1 = add2(G1, valid ? g1 : kZero);
+        const f32x2 e0 = f2(ex2_approx(f2lo(G0)), ex2_approx(f2hi(G0)));
+        const f32x2 e1 = f2(ex2_approx(f2lo(G1)), ex2_approx(f2hi(G1)));
+        const f32x2 r0 = f2(ex2_approx(-f2lo(G0)), ex2_approx(-f2hi(G0)));
+        const f32x2 r1 = f2(ex2_approx(-f2lo(G1)), ex2_approx(-f2hi(G1)));
+        const f32x2 kh0 = mul2(k0, r0), kh1 = mul2(k1, r1);
+        *(uint2*)(sl + SL_XB + sw256(t, 4 * lane)) =
+            make_uint2(f2_to_bf2(mul2(k0, e0)), f2_to_bf2(mul2(k1, e1)));
+        *(uint2*)(sl + SL_XB + sw256(16 + t, 4 * lane)) =
+            make_uint2(f2_to_bf2(mul2(q0, e0)), f2_to_bf2(mul2(q1, e1)));
+        *(uint2*)(kh + sw256(t, 4 * lane)) = make_uint2(f2_to_bf2(kh0), f2_to_bf2(kh1));
+        khr[t][0] = kh0;
+        khr[t][1] = kh1;
+        const f32x2 qk = fma2(q1, k1, mul2(q0, k0));
+        dq[t] = f2lo(qk) + f2hi(qk);
+      }
+      {
+        const f32x2 c0 = f2(ex2_approx(f2lo(G0)), ex2_approx(f2hi(G0)));
+        const f32x2 c1 = f2(ex2_approx(f2lo(G1)), ex2_approx(f2hi(G1)));
+        *(float4*)(sl + SL_EGC + 16 * lane) = make_float4(f2lo(c0), f2hi(c0), f2lo(c1), f2hi(c1));
+#pragma unroll
+        for (int t = 0; t < C; ++t)
+          *(uint2*)(sl + SL_KC + sw256(t, 4 * lane)) =
+              make_uint2(f2_to_bf2(mul2(khr[t][0], c0)), f2_to_bf2(mul2(khr[t][1], c1)));
+      }
+      // V into the slot (swizzled); rows past the end of the sequence are zero
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i, row = e >> 4, c16 = e & 15;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (row < nvalid) val = *(const uint4*)(st + 3 * TILE + row * 256 + c16 * 16);
+        *(uint4*)(sl + SL_V + row * 256 + (((c16 ^ row) & 7) | (c16 & 8)) * 16) = val;
+      }
+      // q_t . k_t: transpose-reduce the 16 per-lane partial sums over the warp;
+      // lane l ends with token (l >> 1) & 15
+      {
+        float v8[8], v4[4], v2[2], v1;
+        const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          v8[j] = (b4 ? dq[j + 8] : dq[j]) + __shfl_xor_sync(0xffffffffu, b4 ? dq[j] : dq[j + 8], 16);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          v4[j] = (b3 ? v8[j + 4] : v8[j]) + __shfl_xor_sync(0xffffffffu, b3 ? v8[j] : v8[j + 4], 8);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          v2[j] = (b2 ? v4[j + 2] : v4[j]) + __shfl_xor_sync(0xffffffffu, b2 ? v4[j] : v4[j + 2], 4);
+        v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+        if ((lane & 1) == 0) ((float*)(sl + SL_DC))[(lane >> 1) & 15] = v1;
+      }
+      // every lane has consumed its reads of the stage: refill it with this
+      // warp's next chunk
+      __syncwarp();
+      if (lane == 0) KTRACE(n, 7);
+      if (n + kIntraWarps < nchunks) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          load(n + kIntraWarps);
+        }
+        ++issued;
+      }
+      // ---- phase B: A = Kt Kh^T and P = Qt Kh^T (M = N = 16, K = 128)
+      float accA[2][4], accP[2][4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) accA[j][c] = accP[j][c] = 0.0f;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t akt[4], aqt[4], b[4];
+        ldmatrix_x4(sls + SL_XB + sw256(rr + 8 * (mi & 1), 16 * kk + 8 * (mi >> 1)), akt[0], akt[1],
+                    akt[2], akt[3]);
+        ldmatrix_x4(sls + SL_XB + sw256(16 + rr + 8 * (mi & 1), 16 * kk + 8 * (mi >> 1)), aqt[0],
+                    aqt[1], aqt[2], aqt[3]);
+        ldmatrix_x4(khs + sw256(rr + 8 * (mi >> 1), 16 * kk + 8 * (mi & 1)), b[0], b[1], b[2], b[3]);
+        mma16816(accA[0], akt, b[0], b[1]);
+        mma16816(accA[1], akt, b[2], b[3]);
+        mma16816(accP[0], aqt, b[0], b[1]);
+        mma16816(accP[1], aqt, b[2], b[3]);
+      }
+      {
+        const float br0 = __shfl_sync(0xffffffffu, beta_l, g);
+        const float br1 = __shfl_sync(0xffffffffu, beta_l, g + 8);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int s0 = 8 * j + 2 * q;
+          // rows g and g + 8; columns s0, s0 + 1; strictly lower parts only
+          *(float2*)(ab + g * C + s0) =
+              make_float2(s0 < g ? br0 * accA[j][0] : 0.0f, s0 + 1 < g ? br0 * accA[j][1] : 0.0f);
+          *(float2*)(ab + (g + 8) * C + s0) = make_float2(
+              s0 < g + 8 ? br1 * accA[j][2] : 0.0f, s0 + 1 < g + 8 ? br1 * accA[j][3] : 0.0f);
+          *(uint32_t*)(sl + SL_P + sw32(g, s0)) =
+              pack_bf16x2(s0 < g ? accP[j][0] : 0.0f, s0 + 1 < g ? accP[j][1] : 0.0f);
+          *(uint32_t*)(sl + SL_P + sw32(g + 8, s0)) =
+              pack_bf16x2(s0 < g + 8 ? accP[j][2] : 0.0f, s0 + 1 < g + 8 ? accP[j][3] : 0.0f);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) KTRACE(n, 8);
+      if (lane < C) {
+        // column j of (I + A)^{-1} by forward substitution, scaled by beta_j
+        const int j = lane;
+        float t[C];
+#pragma unroll
+        for (int i = 0; i < C; ++i) t[i] = (i == j) ? 1.0f : 0.0f;
+#pragma unroll
+        for (int i = 1; i < C; ++i) {
+          float acc0 = 0.0f, acc1 = 0.0f;
+#pragma unroll
+          for (int m4 = 0; m4 < i; m4 += 4) {
+            const float4 a4 = *(const float4*)(ab + i * C + m4);
+            acc0 = fmaf(a4.x, t[m4], acc0);
+            if (m4 + 1 < i) acc1 = fmaf(a4.y, t[m4 + 1], acc1);
+            if (m4 + 2 < i) acc0 = fmaf(a4.z, t[m4 + 2], acc0);
+            if (m4 + 3 < i) acc1 = fmaf(a4.w, t[m4 + 3], acc1);
+          }
+          if (i > j) t[i] = -(acc0 + acc1);
+        }
+#pragma unroll
+        for (int i = 0; i < C; ++i)
+          *(__nv_bfloat16*)(sl + SL_TB + sw32(i, j)) = __float2bfloat16_rn(t[i] * beta_l);
+      }
+      __syncwarp();
+      if (lane == 0) KTRACE(n, 9);
+      // W = Tb Kt (M = 16, N = 128, K = 16); -W then replaces Kt in the slot
+      {
+        uint32_t atb[4];
+        ldmatrix_x4(sls + SL_TB + sw32(rr + 8 * (mi & 1), 8 * (mi >> 1)), atb[0], atb[1], atb[2],
+                    atb[3]);
+        float accW[D / 8][4];
+#pragma unroll
+        for (int p = 0; p < D / 16; ++p) {
+          uint32_t b[4];
+          ldmatrix_x4_trans(sls + SL_XB + sw256(rr + 8 * (mi & 1), 16 * p + 8 * (mi >> 1)), b[0],
+                            b[1], b[2], b[3]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) accW[2 * p][c] = accW[2 * p + 1][c] = 0.0f;
+          mma16816(accW[2 * p], atb, b[0], b[1]);
+          mma16816(accW[2 * p + 1], atb, b[2], b[3]);
+        }
+        __syncwarp();  // all reads of Kt are done before -W overwrites it
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+          *(uint32_t*)(sl + SL_XB + sw256(g, 8 * nt + 2 * q)) =
+              pack_bf16x2(-accW[nt][0], -accW[nt][1]);
+          *(uint32_t*)(sl + SL_XB + sw256(g + 8, 8 * nt + 2 * q)) =
+              pack_bf16x2(-accW[nt][2], -accW[nt][3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[B_READY + slot]);
+        KTRACE(n, 10);
+      }
+    }
+    if (bad) fail(abort, args.status);
+    // a refill issued for a chunk this warp never waited for is drained
+    // before the CTA releases its shared memory
+    if (lane == 0 && issued > consumed) mbar_wait_drain(full, consumed & 1, kWaitNs);
+  } else {
+    // ================================================================ state warps
+    const int sw = warp;
+    const int64_t soff = ((int64_t)ch.seq * H + h) * D * D;
+    // S[m][nt][c]: S^T element (value channel 32 sw + 16 m + g + 8 (c >> 1),
+    // key channel 8 nt + 2 q + (c & 1)) -- the m16n8 accumulator layout
+    float S[2][D / 8][4];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int dv = 32 * sw + 16 * m + g + 8 * (c >> 1), dk = 8 * nt + 2 * q + (c & 1);
+          S[m][nt][c] = args.init_state ? args.init_state[soff + (int64_t)dk * D + dv] : 0.0f;
+        }
+    bool bad = false;
+    for (int n = 0; n < nchunks; ++n) {
+      const int slot = n % NSLOT;
+      const unsigned char* sl = sm + SM_SLOTS + slot * SLOT_BYTES;
+      const uint32_t sls = sbase + SM_SLOTS + slot * SLOT_BYTES;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&bars[B_READY + slot], (n / NSLOT) & 1, abort, kWaitNs))) {
+        bad = true;
+        break;
+      }
+      if (tid == 0) {
+        KTRACE(n, 0);
+        KTRACE_CLK(n, 15);
+      }
+      // ---- [U' | 0] = V^T Tb^T
+      float accU[2][2][4], accO[2][2][4];
+      {
+        uint32_t tb[4];
+        ldmatrix_x4(sls + SL_TB + sw32(rr + 8 * (mi >> 1), 8 * (mi & 1)), tb[0], tb[1], tb[2], tb[3]);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          uint32_t a[4];
+          ldmatrix_x4_trans(sls + SL_V + sw256(rr + 8 * (mi >> 1), 32 * sw + 16 * m + 8 * (mi & 1)),
+                            a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) accU[m][j][c] = accO[m][j][c] = 0.0f;
+          mma16816(accU[m][0], a, tb[0], tb[1]);
+          mma16816(accU[m][1], a, tb[2], tb[3]);
+        }
+      }
+      // ---- [U | O] += S^T [-W | Qt]^T; S is rounded to bf16 for the product
+      // and then scaled by e^{G_C} in place
+      const float* egc = (const float*)(sl + SL_EGC);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t bw[4], bq[4];
+        ldmatrix_x4(sls + SL_XB + sw256(rr + 8 * (mi >> 1), 16 * kk + 8 * (mi & 1)), bw[0], bw[1],
+                    bw[2], bw[3]);
+        ldmatrix_x4(sls + SL_XB + sw256(16 + rr + 8 * (mi >> 1), 16 * kk + 8 * (mi & 1)), bq[0],
+                    bq[1], bq[2], bq[3]);
+        const float2 e0 = *(const float2*)(egc + 16 * kk + 2 * q);
+        const float2 e1 = *(const float2*)(egc + 16 * kk + 8 + 2 * q);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          float* s0 = S[m][2 * kk];
+          float* s1 = S[m][2 * kk + 1];
+          const uint32_t a[4] = {pack_bf16x2(s0[0], s0[1]), pack_bf16x2(s0[2], s0[3]),
+                                 pack_bf16x2(s1[0], s1[1]), pack_bf16x2(s1[2], s1[3])};
+          s0[0] *= e0.x;
+          s0[1] *= e0.y;
+          s0[2] *= e0.x;
+          s0[3] *= e0.y;
+          s1[0] *= e1.x;
+          s1[1] *= e1.y;
+          s1[2] *= e1.x;
+          s1[3] *= e1.y;
+          mma16816(accU[m][0], a, bw[0], bw[1]);
+          mma16816(accU[m][1], a, bw[2], bw[3]);
+          mma16816(accO[m][0], a, bq[0], bq[1]);
+          mma16816(accO[m][1], a, bq[2], bq[3]);
+        }
+      }
+      // ---- U as a bf16 high/low pair of A fragments
+      uint32_t uh[2][4], ul[2][4];
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            const float x0 = accU[m][j][2 * p], x1 = accU[m][j][2 * p + 1];
+            const uint32_t hi = pack_bf16x2(x0, x1);
+            const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&hi);
+            uh[m][2 * j + p] = hi;
+            ul[m][2 * j + p] = pack_bf16x2(x0 - __low2float(hb), x1 - __high2float(hb));
+          }
+      if (tid == 0) KTRACE(n, 2);
+      // ---- O += U^T P^T + Diag(q.k) U, then the outputs of the chunk
+      {
+        uint32_t pb[4];
+        ldmatrix_x4(sls + SL_P + sw32(rr + 8 * (mi >> 1), 8 * (mi & 1)), pb[0], pb[1], pb[2], pb[3]);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          mma16816(accO[m][0], uh[m], pb[0], pb[1]);
+          mma16816(accO[m][1], uh[m], pb[2], pb[3]);
+          mma16816(accO[m][0], ul[m], pb[0], pb[1]);
+          mma16816(accO[m][1], ul[m], pb[2], pb[3]);
+        }
+        const float* dc = (const float*)(sl + SL_DC);
+        const float2 dc0 = *(const float2*)(dc + 2 * q), dc1 = *(const float2*)(dc + 8 + 2 * q);
+        const int nvalid = min(C, L - n * C);
+        const int64_t row0 = ch.t0 + (int64_t)n * C;
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int r = 8 * j + 2 * q + (c & 1);
+              const int dv = 32 * sw + 16 * m + g + 8 * (c >> 1);
+              const float dcr = j ? ((c & 1) ? dc1.y : dc1.x) : ((c & 1) ? dc0.y : dc0.x);
+              const float o = accO[m][j][c] + dcr * accU[m][j][c];
+              if (r < nvalid) {
+                const int64_t idx = ((row0 + r) * H + h) * D + dv;
+                if (args.out_bf16)
+                  ((__nv_bfloat16*)args.out)[idx] = __float2bfloat16_rn(o);
+                else
+                  ((float*)args.out)[idx] = o;
+              }
+            }
+      }
+      if (tid == 0) KTRACE(n, 3);
+      // ---- S^T += U^T KhC (K = 16).  Inside the sequence U enters as bf16:
+      // the outputs do not see the difference (they sum over 128 key
+      // channels and every chunk decays the state), but the final state is
+      // returned element by element, so the last chunk adds the low part too.
+#pragma unroll
+      for (int p = 0; p < D / 16; ++p) {
+        uint32_t b[4];
+        ldmatrix_x4_trans(sls + SL_KC + sw256(rr + 8 * (mi & 1), 16 * p + 8 * (mi >> 1)), b[0], b[1],
+                          b[2], b[3]);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          mma16816(S[m][2 * p], uh[m], b[0], b[1]);
+          mma16816(S[m][2 * p + 1], uh[m], b[2], b[3]);
+        }
+      }
+      if (n + 1 == nchunks) {
+#pragma unroll
+        for (int p = 0; p < D / 16; ++p) {
+          uint32_t b[4];
+          ldmatrix_x4_trans(sls + SL_KC + sw256(rr + 8 * (mi & 1), 16 * p + 8 * (mi >> 1)), b[0],
+                            b[1], b[2], b[3]);
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            mma16816(S[m][2 * p], ul[m], b[0], b[1]);
+            mma16816(S[m][2 * p + 1], ul[m], b[2], b[3]);
+          }
+        }
+      }
+      // the slot's reads are all consumed (their values fed the products above)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_FREE + slot]);
+      if (tid == 0) KTRACE(n, 4);
+    }
+    if (bad) fail(abort, args.status);
+    if (!bad && args.final_state) {
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int dv = 32 * sw + 16 * m + g + 8 * (c >> 1), dk = 8 * nt + 2 * q + (c & 1);
+            args.final_state[soff + (int64_t)dk * D + dv] = S[m][nt][c];
+          }
+    }
+  }
+}
+
+}  // namespace
+
+bool mma_supported(int dtype, int dk, int dv) {
+  return dtype == KDA_DTYPE_BF16 && dk == D && dv == D;
+}
+
+int launch_mma(const FwdParams& p, cudaStream_t stream) {
+  if (!mma_supported(p.dtype, p.dk, p.dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
+  const int64_t tokens = p.cu_seqlens ? (int64_t)p.T : (int64_t)p.N * p.T;
+  if (tokens <= 0) {
+    // nothing to load; a tensor map needs a nonzero extent, so use the SIMT
+    // kernel, which handles empty sequences with no loads
+    return launch_simt(p, stream);
+  }
+  if (tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;
+  CUtensorMap mq, mk, mth, mv;
+  if (!encode_token_rows(&mq, p.q, p.H, tokens) || !encode_token_rows(&mk, p.k, p.H, tokens) ||
+      !encode_token_rows(&mth, p.theta, p.H, tokens) || !encode_token_rows(&mv, p.v, p.H, tokens))
+    return KDA_ERR_CUDA;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, []() {
+    attr_err = cudaFuncSetAttribute(kda_fwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return KDA_ERR_LAUNCH;
+  MmaArgs a;
+  a.beta = (const __nv_bfloat16*)p.beta;
+  a.g_min = p.g_min;
+  a.init_state = p.init_state;
+  a.out = p.out;
+  a.out_bf16 = p.out_dtype == KDA_DTYPE_BF16;
+  a.final_state = p.final_state;
+  a.cu_seqlens = p.cu_seqlens;
+  a.N = p.N;
+  a.H = p.H;
+  a.T = p.T;
+  a.status = status_word_device_ptr();
+  if (!a.status) return KDA_ERR_CUDA;
+  kda_fwd_mma_kernel<<<(unsigned)(p.N * p.H), kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+}  // namespace kda
+
+#ifdef KDA_TRACE
+extern "C" KDA_API int kda_debug_trace_read_mma(void* dst, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(dst, kda::g_kda_trace_mma, bytes);
+}
+#endif

@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           stop = true;
           break;
         }
+        if (it == 0) KTRACE(n, 9);
         const f32x2 other = xch[(1 - hf) * 64 + cp];
         if (hf) {
 #pragma unroll
@@ -372,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
+        if (it == 0) KTRACE(n, 14);
         if (bar_sync_or(NB_INTRA, 128, bad || *abort)) {
           stop = true;
           break;
@@ -391,6 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               load_chunk(n + NS);
               issued = n + NS + 1;
             }
+            KTRACE(n, 15);
           }
         }
       }
@@ -728,40 +731,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ---------------------------------------------------------------- host side
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode() {
-  static std::once_flag once;
-  static EncodeTiledFn fn = nullptr;
-  std::call_once(once, []() {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (EncodeTiledFn)p;
-  });
-  return fn;
-}
-
-// [tokens, H, 128] bf16 -> boxes of 16 tokens x 128 channels of one head
-bool encode_rows(CUtensorMap* m, const void* base, int H, int64_t tokens) {
-  EncodeTiledFn enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)tokens};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-  cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 bool tc_supported(int dtype, int dk, int dv) {
@@ -778,8 +747,8 @@ int launch_tc(const FwdParams& p, cudaStream_t stream) {
   }
   if (tokens > INT32_MAX) return KDA_ERR_INVALID_ARG;
   CUtensorMap mq, mk, mth, mv;
-  if (!encode_rows(&mq, p.q, p.H, tokens) || !encode_rows(&mk, p.k, p.H, tokens) ||
-      !encode_rows(&mth, p.theta, p.H, tokens) || !encode_rows(&mv, p.v, p.H, tokens))
+  if (!encode_token_rows(&mq, p.q, p.H, tokens) || !encode_token_rows(&mk, p.k, p.H, tokens) ||
+      !encode_token_rows(&mth, p.theta, p.H, tokens) || !encode_token_rows(&mv, p.v, p.H, tokens))
     return KDA_ERR_CUDA;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;

@@ -25,7 +25,7 @@ KDA_ERR_DEVICE_TIMEOUT = -5
 KDA_ERR_CUDA = -6
 KDA_ERR_UNSUPPORTED_SHAPE = -7
 
-PATHS = {"auto": 0, "simt": 1, "tc": 2}
+PATHS = {"auto": 0, "simt": 1, "tc": 2, "mma": 3}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
 _lock = threading.Lock()

@@ -82,4 +82,5 @@ def test_select_path_host_logic():
     assert lib.kda_select_path(1, 16, 16) == 1          # fp32 -> SIMT
     assert lib.kda_select_path(0, 24, 128) == binding.KDA_ERR_UNSUPPORTED_SHAPE
     assert lib.kda_select_path(5, 128, 128) == binding.KDA_ERR_INVALID_ARG
-    assert lib.kda_select_path(0, 64, 64) == 1          # bf16 off the TC shape -> SIMT
+    assert lib.kda_select_path(0, 64, 64) == 1          # bf16 off the 128 x 128 shape -> SIMT
+    assert lib.kda_select_path(0, 128, 128) == 3        # bf16, dk = dv = 128 -> register-resident path

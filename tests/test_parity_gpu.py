@@ -19,8 +19,8 @@ def _paths(dtype, dk, dv):
     if dtype == torch.float32:
         return ["simt"]
     ps = ["simt"]
-    if kda_select_path(dtype, dk, dv) == "tc":
-        ps.append("tc")
+    if dk == 128 and dv == 128:
+        ps += ["tc", "mma"]
     return ps
 
 
@@ -150,7 +150,7 @@ def test_decay_stress_small(path):
     _check_full(w, inp, path)
 
 
-@pytest.mark.parametrize("path", ["simt"] + (["tc"] if len(_bf16_paths()) > 1 else []))
+@pytest.mark.parametrize("path", _bf16_paths())
 def test_null_states_and_continuation(path):
     w, inp = _custom(B=2, H=2, T=96, init=0.0, seed=31)
     g = _to(inp, "cuda")
