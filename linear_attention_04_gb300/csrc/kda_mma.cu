@@ -65,8 +65,15 @@ using namespace sm100;
 constexpr int C = kChunk;  // 16
 constexpr int D = 128;     // dk = dv
 constexpr int kStateWarps = 4;
+constexpr int kDvPerWarp = D / kStateWarps;  // value channels per state warp
+constexpr int kMT = kDvPerWarp / 16;          // m16 tiles per state warp
+static_assert(kMT >= 1 && kMT * 16 * kStateWarps == D, "state warp split");
 constexpr int kIntraWarps = 4;
 constexpr int kThreads = 32 * (kStateWarps + kIntraWarps);
+// Per-thread registers of each role after setmaxnreg (0: every warp keeps the
+// launch allocation).  The split must fit the launch allocation; the host
+// checks it against the compiled register count before the first launch.
+constexpr int kStateRegs = 0, kIntraRegs = 0;
 constexpr int NSLOT = 6;  // chunk slots between the intra and the state warps
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
@@ -125,6 +132,17 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Register count of every thread at launch (the full file divided evenly) and
+// the per-role adjustment away from it.
+constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8 > 255 ? 255 : (65536 / kThreads) / 8 * 8;
+template <int N>
+__device__ __forceinline__ void set_regs() {
+  if constexpr (N > kLaunchRegs)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+  else if constexpr (N < kLaunchRegs)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 struct MmaArgs {
   const __nv_bfloat16* beta;
   float g_min;
@@ -164,6 +182,7 @@ __device__ __forceinline__ void fail(volatile int* abort, int* status) {
   atomicExch(status, KDA_ERR_DEVICE_TIMEOUT);
 }
 
+template <bool kOutBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_fwd_mma_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -195,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kStateWarps) {
     // ================================================================ intra warps
+    if constexpr (kIntraRegs > 0) set_regs<kIntraRegs>();
     const int iw = warp - kStateWarps;
     unsigned char* st = sm + SM_RING + iw * STAGE;
     const uint32_t khs = sbase + SM_KH + iw * TILE;
@@ -244,6 +264,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (lane == 0) KTRACE(n, 6);
+      if (nvalid < C) {
+        // rows past the end of the sequence (the next sequence's tokens, or the
+        // zero fill past the tensor) become neutral: q = k = v = 0 and
+        // theta = -inf, i.e. g = 0 (no decay) and no contribution
+        for (int e = lane; e < (C - nvalid) * 16; e += 32) {
+          const int row = nvalid + (e >> 4), c16 = e & 15;
+          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          const uint4 ninf = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+          *(uint4*)(st + 0 * TILE + row * 256 + c16 * 16) = z;
+          *(uint4*)(st + 1 * TILE + row * 256 + c16 * 16) = z;
+          *(uint4*)(st + 2 * TILE + row * 256 + c16 * 16) = ninf;
+          *(uint4*)(st + 3 * TILE + row * 256 + c16 * 16) = z;
+        }
+        __syncwarp();
+      }
       // ---- phase A: gate, cumulative sums, decayed operands.  Lane l holds
       // channels 4l .. 4l+3 of every token of the chunk.
       const uint2* sq = (const uint2*)(st + 0 * TILE);
@@ -254,17 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       float dq[C];                   // partial q_t . k_t over this lane's channels
 #pragma unroll
       for (int t = 0; t < C; ++t) {
-        const bool valid = t < nvalid;
         const uint2 thw = sth[t * 32 + lane], kw = sk[t * 32 + lane], qw = sq[t * 32 + lane];
-        const f32x2 k0 = valid ? bf2_to_f2(kw.x) : kZero, k1 = valid ? bf2_to_f2(kw.y) : kZero;
-        const f32x2 q0 = valid ? bf2_to_f2(qw.x) : kZero, q1 = valid ? bf2_to_f2(qw.y) : kZero;
+        const f32x2 k0 = bf2_to_f2(kw.x), k1 = bf2_to_f2(kw.y);
+        const f32x2 q0 = bf2_to_f2(qw.x), q1 = bf2_to_f2(qw.y);
         const f32x2 x0 = mul2(bf2_to_f2(thw.x), kC2), x1 = mul2(bf2_to_f2(thw.y), kC2);
         const f32x2 d0 = add2(f2(ex2_approx(f2lo(x0)), ex2_approx(f2hi(x0))), kOne);
         const f32x2 d1 = add2(f2(ex2_approx(f2lo(x1)), ex2_approx(f2hi(x1))), kOne);
         const f32x2 g0 = mul2(f2(rcp_approx(f2lo(d0)), rcp_approx(f2hi(d0))), kC1);
         const f32x2 g1 = mul2(f2(rcp_approx(f2lo(d1)), rcp_approx(f2hi(d1))), kC1);
-        G0 = add2(G0, valid ? g0 : kZero);
-        G1 = add2(G1, valid ? g1 : kZero);
+        G0 = add2(G0, g0);
+        G1 = add2(G1, g1);
         const f32x2 e0 = f2(ex2_approx(f2lo(G0)), ex2_approx(f2hi(G0)));
         const f32x2 e1 = f2(ex2_approx(f2lo(G1)), ex2_approx(f2hi(G1)));
         const f32x2 r0 = f2(ex2_approx(-f2lo(G0)), ex2_approx(-f2hi(G0)));
@@ -289,13 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           *(uint2*)(sl + SL_KC + sw256(t, 4 * lane)) =
               make_uint2(f2_to_bf2(mul2(khr[t][0], c0)), f2_to_bf2(mul2(khr[t][1], c1)));
       }
-      // V into the slot (swizzled); rows past the end of the sequence are zero
+      // V into the slot (swizzled)
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int e = lane + 32 * i, row = e >> 4, c16 = e & 15;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (row < nvalid) val = *(const uint4*)(st + 3 * TILE + row * 256 + c16 * 16);
-        *(uint4*)(sl + SL_V + row * 256 + (((c16 ^ row) & 7) | (c16 & 8)) * 16) = val;
+        *(uint4*)(sl + SL_V + row * 256 + (((c16 ^ row) & 7) | (c16 & 8)) * 16) =
+            *(const uint4*)(st + 3 * TILE + row * 256 + c16 * 16);
       }
       // q_t . k_t: transpose-reduce the 16 per-lane partial sums over the warp;
       // lane l ends with token (l >> 1) & 15
@@ -426,18 +459,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && issued > consumed) mbar_wait_drain(full, consumed & 1, kWaitNs);
   } else {
     // ================================================================ state warps
+    if constexpr (kStateRegs > 0) set_regs<kStateRegs>();
     const int sw = warp;
     const int64_t soff = ((int64_t)ch.seq * H + h) * D * D;
     // S[m][nt][c]: S^T element (value channel 32 sw + 16 m + g + 8 (c >> 1),
     // key channel 8 nt + 2 q + (c & 1)) -- the m16n8 accumulator layout
-    float S[2][D / 8][4];
+    float S[kMT][D / 8][4];
 #pragma unroll
-    for (int m = 0; m < 2; ++m)
+    for (int m = 0; m < kMT; ++m)
 #pragma unroll
       for (int nt = 0; nt < D / 8; ++nt)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int dv = 32 * sw + 16 * m + g + 8 * (c >> 1), dk = 8 * nt + 2 * q + (c & 1);
+          const int dv = kDvPerWarp * sw + 16 * m + g + 8 * (c >> 1), dk = 8 * nt + 2 * q + (c & 1);
           S[m][nt][c] = args.init_state ? args.init_state[soff + (int64_t)dk * D + dv] : 0.0f;
         }
     bool bad = false;
@@ -455,14 +489,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         KTRACE_CLK(n, 15);
       }
       // ---- [U' | 0] = V^T Tb^T
-      float accU[2][2][4], accO[2][2][4];
+      float accU[kMT][2][4], accO[kMT][2][4];
       {
         uint32_t tb[4];
         ldmatrix_x4(sls + SL_TB + sw32(rr + 8 * (mi >> 1), 8 * (mi & 1)), tb[0], tb[1], tb[2], tb[3]);
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
+        for (int m = 0; m < kMT; ++m) {
           uint32_t a[4];
-          ldmatrix_x4_trans(sls + SL_V + sw256(rr + 8 * (mi >> 1), 32 * sw + 16 * m + 8 * (mi & 1)),
+          ldmatrix_x4_trans(sls + SL_V + sw256(rr + 8 * (mi >> 1), kDvPerWarp * sw + 16 * m + 8 * (mi & 1)),
                             a[0], a[1], a[2], a[3]);
 #pragma unroll
           for (int j = 0; j < 2; ++j)
@@ -485,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 e0 = *(const float2*)(egc + 16 * kk + 2 * q);
         const float2 e1 = *(const float2*)(egc + 16 * kk + 8 + 2 * q);
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
+        for (int m = 0; m < kMT; ++m) {
           float* s0 = S[m][2 * kk];
           float* s1 = S[m][2 * kk + 1];
           const uint32_t a[4] = {pack_bf16x2(s0[0], s0[1]), pack_bf16x2(s0[2], s0[3]),
@@ -505,9 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // ---- U as a bf16 high/low pair of A fragments
-      uint32_t uh[2][4], ul[2][4];
+      uint32_t uh[kMT][4], ul[kMT][4];
 #pragma unroll
-      for (int m = 0; m < 2; ++m)
+      for (int m = 0; m < kMT; ++m)
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -519,41 +553,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ul[m][2 * j + p] = pack_bf16x2(x0 - __low2float(hb), x1 - __high2float(hb));
           }
       if (tid == 0) KTRACE(n, 2);
-      // ---- O += U^T P^T + Diag(q.k) U, then the outputs of the chunk
+      // ---- O += U^T P^T
       {
         uint32_t pb[4];
         ldmatrix_x4(sls + SL_P + sw32(rr + 8 * (mi >> 1), 8 * (mi & 1)), pb[0], pb[1], pb[2], pb[3]);
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
+        for (int m = 0; m < kMT; ++m) {
           mma16816(accO[m][0], uh[m], pb[0], pb[1]);
           mma16816(accO[m][1], uh[m], pb[2], pb[3]);
           mma16816(accO[m][0], ul[m], pb[0], pb[1]);
           mma16816(accO[m][1], ul[m], pb[2], pb[3]);
         }
-        const float* dc = (const float*)(sl + SL_DC);
-        const float2 dc0 = *(const float2*)(dc + 2 * q), dc1 = *(const float2*)(dc + 8 + 2 * q);
-        const int nvalid = min(C, L - n * C);
-        const int64_t row0 = ch.t0 + (int64_t)n * C;
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int r = 8 * j + 2 * q + (c & 1);
-              const int dv = 32 * sw + 16 * m + g + 8 * (c >> 1);
-              const float dcr = j ? ((c & 1) ? dc1.y : dc1.x) : ((c & 1) ? dc0.y : dc0.x);
-              const float o = accO[m][j][c] + dcr * accU[m][j][c];
-              if (r < nvalid) {
-                const int64_t idx = ((row0 + r) * H + h) * D + dv;
-                if (args.out_bf16)
-                  ((__nv_bfloat16*)args.out)[idx] = __float2bfloat16_rn(o);
-                else
-                  ((float*)args.out)[idx] = o;
-              }
-            }
       }
-      if (tid == 0) KTRACE(n, 3);
       // ---- S^T += U^T KhC (K = 16).  Inside the sequence U enters as bf16:
       // the outputs do not see the difference (they sum over 128 key
       // channels and every chunk decays the state), but the final state is
@@ -564,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ldmatrix_x4_trans(sls + SL_KC + sw256(rr + 8 * (mi & 1), 16 * p + 8 * (mi >> 1)), b[0], b[1],
                           b[2], b[3]);
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
+        for (int m = 0; m < kMT; ++m) {
           mma16816(S[m][2 * p], uh[m], b[0], b[1]);
           mma16816(S[m][2 * p + 1], uh[m], b[2], b[3]);
         }
@@ -576,11 +587,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           ldmatrix_x4_trans(sls + SL_KC + sw256(rr + 8 * (mi & 1), 16 * p + 8 * (mi >> 1)), b[0],
                             b[1], b[2], b[3]);
 #pragma unroll
-          for (int m = 0; m < 2; ++m) {
+          for (int m = 0; m < kMT; ++m) {
             mma16816(S[m][2 * p], ul[m], b[0], b[1]);
             mma16816(S[m][2 * p + 1], ul[m], b[2], b[3]);
           }
         }
+      }
+      if (tid == 0) KTRACE(n, 3);
+      // ---- outputs of the chunk: O + Diag(q.k) U (after the state products
+      // are issued, so that the tensor pipe works while the stores go out)
+      {
+        const float* dc = (const float*)(sl + SL_DC);
+        const float2 dc0 = *(const float2*)(dc + 2 * q), dc1 = *(const float2*)(dc + 8 + 2 * q);
+        const int nvalid = min(C, L - n * C);
+        const int64_t row0 = ch.t0 + (int64_t)n * C;
+#pragma unroll
+        for (int m = 0; m < kMT; ++m)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int r = 8 * j + 2 * q + (c & 1);
+              const int dv = kDvPerWarp * sw + 16 * m + g + 8 * (c >> 1);
+              const float dcr = j ? ((c & 1) ? dc1.y : dc1.x) : ((c & 1) ? dc0.y : dc0.x);
+              const float o = accO[m][j][c] + dcr * accU[m][j][c];
+              if (r < nvalid) {
+                const int64_t idx = ((row0 + r) * H + h) * D + dv;
+                if constexpr (kOutBf16)
+                  ((__nv_bfloat16*)args.out)[idx] = __float2bfloat16_rn(o);
+                else
+                  ((float*)args.out)[idx] = o;
+              }
+            }
       }
       // the slot's reads are all consumed (their values fed the products above)
       __syncwarp();
@@ -590,12 +628,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (bad) fail(abort, args.status);
     if (!bad && args.final_state) {
 #pragma unroll
-      for (int m = 0; m < 2; ++m)
+      for (int m = 0; m < kMT; ++m)
 #pragma unroll
         for (int nt = 0; nt < D / 8; ++nt)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const int dv = 32 * sw + 16 * m + g + 8 * (c >> 1), dk = 8 * nt + 2 * q + (c & 1);
+            const int dv = kDvPerWarp * sw + 16 * m + g + 8 * (c >> 1), dk = 8 * nt + 2 * q + (c & 1);
             args.final_state[soff + (int64_t)dk * D + dv] = S[m][nt][c];
           }
     }
@@ -624,8 +662,19 @@ int launch_mma(const FwdParams& p, cudaStream_t stream) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, []() {
-    attr_err = cudaFuncSetAttribute(kda_fwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)SMEM_BYTES);
+    for (const void* fn : {(const void*)kda_fwd_mma_kernel<false>, (const void*)kda_fwd_mma_kernel<true>}) {
+      if (attr_err == cudaSuccess)
+        attr_err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+      if (kStateRegs > 0 && attr_err == cudaSuccess) {
+        // setmaxnreg.inc can only draw on the registers the block was launched
+        // with: a split above the compiled launch allocation would wait forever
+        cudaFuncAttributes fa;
+        attr_err = cudaFuncGetAttributes(&fa, fn);
+        if (attr_err == cudaSuccess &&
+            kStateWarps * kStateRegs + kIntraWarps * kIntraRegs > fa.numRegs * (kThreads / 32))
+          attr_err = cudaErrorInvalidConfiguration;
+      }
+    }
   });
   if (attr_err != cudaSuccess) return KDA_ERR_LAUNCH;
   MmaArgs a;
@@ -641,7 +690,10 @@ int launch_mma(const FwdParams& p, cudaStream_t stream) {
   a.T = p.T;
   a.status = status_word_device_ptr();
   if (!a.status) return KDA_ERR_CUDA;
-  kda_fwd_mma_kernel<<<(unsigned)(p.N * p.H), kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
+  if (a.out_bf16)
+    kda_fwd_mma_kernel<true><<<(unsigned)(p.N * p.H), kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
+  else
+    kda_fwd_mma_kernel<false><<<(unsigned)(p.N * p.H), kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
