@@ -19,6 +19,7 @@ only), each step a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import glob
 import hashlib
 import json
@@ -257,12 +258,23 @@ def cpu_baseline(w: Workload, target_s: float, seed: int) -> dict:
 
 # ----------------------------------------------------------------------------- our arm
 
+def selected_workload(args):
+    """The named workload, with B replaced when --batch is given (smaller
+    profiling cases of the same shape per sequence)."""
+    w = WORKLOADS[args.workload]
+    if args.batch:
+        if w.varlen:
+            raise SystemExit("--batch applies to fixed-length workloads only")
+        w = dataclasses.replace(w, B=args.batch)
+    return w
+
+
 def run_ours(args, rank, world, local):
     from linear_attention_04_gb300 import kda_chunk_fwd, kda_device_status, kda_select_path
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = WORKLOADS[args.workload]
+    w = selected_workload(args)
     inp = make_inputs(w, seed=rank_seed(args.seed, rank), device=dev)
     q, k, v, th, be = inp["q"], inp["k"], inp["v"], inp["theta"], inp["beta"]
     init, cu = inp["init_state"], inp["cu_seqlens"]
@@ -402,7 +414,7 @@ def run_ours(args, rank, world, local):
 
 def run_reference(args, rank, world):
     import oracle
-    w = WORKLOADS[args.workload]
+    w = selected_workload(args)
     oracle.build()
     threads = oracle.host_threads()
     # size one step's sample to about args.ref_step_seconds of oracle work
@@ -444,6 +456,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="train_bf16")
     ap.add_argument("--path", choices=["auto", "simt", "tc", "mma"], default="auto")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="replace the workload's B (fixed-length workloads; profiling cases)")
     ap.add_argument("--seed", type=int, default=20261204)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
