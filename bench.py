@@ -448,6 +448,82 @@ def run_reference(args, rank, world):
 
 # ----------------------------------------------------------------------------- main
 
+# ----------------------------------------------------------------------------- decode step
+
+DECODE = dict(N=128, H=32, d=128)  # serving-sized batch: 128 sequences x 32 heads, d = 128
+
+
+def decode_bytes(N, H, dk, dv, e=2) -> int:
+    """HBM bytes of one decode step: the fp32 state read and written, the
+    token's q, k, theta, v, beta and the fp32 output."""
+    return N * H * (2 * 4 * dk * dv + e * (3 * dk + dv) + e + 4 * dv)
+
+
+def run_decode(args, rank, world, local):
+    from linear_attention_04_gb300 import kda_decode_step, kda_device_status
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    N, H, d = DECODE["N"], DECODE["H"], DECODE["d"]
+    g = torch.Generator(device="cpu").manual_seed(rank_seed(args.seed, rank))
+    q = torch.nn.functional.normalize(torch.randn(N, H, d, generator=g), dim=-1)
+    k = torch.nn.functional.normalize(torch.randn(N, H, d, generator=g), dim=-1)
+    v = torch.randn(N, H, d, generator=g)
+    th = torch.randn(N, H, d, generator=g)
+    be = torch.sigmoid(torch.randn(N, H, generator=g))
+    q, k, v, th, be = (x.to(dev, torch.bfloat16) for x in (q, k, v, th, be))
+    state = (0.02 * torch.randn(N, H, d, d, generator=g)).to(dev)
+    out = torch.empty((N, H, d), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda_decode_step(q, k, v, th, be, state, -5.0, out, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if kda_device_status(clear=True) != 0:
+        raise RuntimeError("device status after warm-up")
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    gpu_id = str(gpu_id) if gpu_id is not None else str(local)
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) == 36:
+        gpu_id = "GPU-" + gpu_id
+    clocks = ClockSampler(gpu_id).start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    time.sleep(0.25)
+    clocks.stop()
+    total_ms = max_over_ranks(start.elapsed_time(end), world)
+    step_s = total_ms / args.steps / 1e3
+    peaks, peak_src = measured_peaks()
+    nbytes = decode_bytes(N, H, d, d)
+    achieved = nbytes / step_s / 1e9
+    return {"metric": "KDA decode tokens/s: one token per sequence against a resident fp32 "
+                      "state, N=128 sequences x H=32 heads, d=128",
+            "value": N * world / step_s, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "op": "decode",
+            "config": {"workload": f"decode: N={N} H={H} d={d}, bf16 token inputs, fp32 state",
+                       "l2": f"state {N * H * d * d * 4 / 1e6:.0f} MB per step vs 126 MB L2"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "traffic": None, "peak_source": f"hbm_gbs of {peak_src}",
+                         "kernel": "kda_decode_kernel", "algorithmic_bytes_per_launch": nbytes},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps,
+            "clocks": clocks.summary(t_wall0, t_wall1)}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -463,6 +539,8 @@ def main(argv=None):
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=["fwd", "decode"], default="fwd",
+                    help="fwd: the chunked forward (the headline); decode: one recurrent step")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("note: at least 3 warm-up steps are required; using 3", file=sys.stderr)
@@ -480,7 +558,7 @@ def main(argv=None):
                 return 0
             line = run_reference(args, rank, world)
         else:
-            line = run_ours(args, rank, world, local)
+            line = (run_decode if args.op == "decode" else run_ours)(args, rank, world, local)
         if rank == 0:
             print(json.dumps(line), flush=True)
     finally:

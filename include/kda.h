@@ -141,6 +141,27 @@ typedef struct kda_fwd_args {
 
 KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* args, cudaStream_t stream);
 
+/*
+ * kda_decode_step -- one recurrent step per (sequence, head): a single new
+ * token against a resident fp32 state, which is updated in place.  The same
+ * recurrence as kda_chunk_fwd for T = 1 ("Kimi K3 Deep Dive", section "Core
+ * Innovation 1"; the fixed-size state of the "Kimi K3" explainer, section
+ * "Across the sequence"):
+ *   g = g_min * sigmoid(theta),  S <- Diag(e^g) S,
+ *   S <- S + beta k (v - S^T k)^T,  o = S^T q.
+ * Layouts (contiguous, row-major): q, k, theta [N, H, dk]; v [N, H, dv];
+ * beta [N, H]; state [N, H, dk, dv] fp32 (dk rows); out [N, H, dv] fp32.
+ * `dtype` (KDA_DTYPE_BF16 or KDA_DTYPE_F32) is the type of q, k, v, theta and
+ * beta; the arithmetic is fp32.  All pointers are device pointers, 16-byte
+ * aligned, owned by the caller; `state` is read and overwritten, `out` fully
+ * written, the inputs only read.  N = 0 is a no-op.  Errors as for
+ * kda_chunk_fwd (returned before anything is queued).  Asynchronous on
+ * `stream`; the library allocates nothing.
+ */
+KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const void* theta,
+                            const void* beta, float g_min, float* state, float* out, int N, int H,
+                            int dk, int dv, int dtype, cudaStream_t stream);
+
 /* Reads the current device's status word (KDA_OK or KDA_ERR_DEVICE_TIMEOUT).
  * Synchronous with respect to the device's prior work only through the copy:
  * call after synchronising the streams that ran the forward pass.  A nonzero

@@ -147,6 +147,38 @@ KDA_API int kda_chunk_fwd_f32(const float* q, const float* k, const float* v, co
   return kda_chunk_fwd_ex(&a, stream);
 }
 
+KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const void* theta,
+                            const void* beta, float g_min, float* state, float* out, int N, int H,
+                            int dk, int dv, int dtype, cudaStream_t stream) {
+  if (N < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+  if (!(g_min < 0.0f) || g_min != g_min) return KDA_ERR_INVALID_ARG;
+  if (!kda::shape_ok(dk) || !kda::shape_ok(dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)N * H > (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
+  if (N > 0 && (!q || !k || !v || !theta || !beta || !state || !out)) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, theta, beta, state, out};
+  for (const void* p : ptrs)
+    if (p && !kda::aligned16(p)) return KDA_ERR_MISALIGNED;
+  if (N == 0) return KDA_OK;
+  const int rc = kda::check_device();
+  if (rc != KDA_OK) return rc;
+  kda::DecodeParams p;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.theta = theta;
+  p.beta = beta;
+  p.g_min = g_min;
+  p.state = state;
+  p.out = out;
+  p.N = N;
+  p.H = H;
+  p.dk = dk;
+  p.dv = dv;
+  p.dtype = dtype;
+  return kda::launch_decode(p, stream);
+}
+
 KDA_API int kda_device_status(int clear) {
   int* p = kda::status_word_device_ptr();
   if (!p) return KDA_ERR_CUDA;

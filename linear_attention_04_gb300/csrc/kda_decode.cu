@@ -1,0 +1,131 @@
+// kda_decode.cu -- recurrent decode step of KDA: one token per (sequence,
+// head) against a resident fp32 state, updated in place.
+//
+// For a single token the chunked form reduces to the recurrence itself
+// ("Kimi K3 Deep Dive", section "Core Innovation 1"; the fixed-size state is
+// what makes the per-token cost independent of the context length, "Kimi K3"
+// explainer, section "Across the sequence"):
+//
+//   g  = g_min * sigmoid(theta)                        (vector over dk)
+//   S <- Diag(e^{g}) S                                 (row scale)
+//   u  = beta (v - S^T k)                              (dv)
+//   S <- S + k u^T                                     ((I - beta k k^T) D S + beta k v^T)
+//   o  = S^T q
+//
+// One CTA per (sequence, head); each thread holds up to 64 key rows of one
+// value column in registers (coalesced across the warp for every key row), so
+// the state is read from HBM once and written once -- the step is bound by
+// those 2 * 4 * dk * dv bytes.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda_device.cuh"
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+// Threads: RG row groups x DV value channels.  Thread (rg, j) keeps rows
+// [rg * DK / RG, (rg + 1) * DK / RG) of column j in registers; the row groups
+// combine their partial sums through shared memory.  With DV a compile-time
+// constant every state access is one base register plus an immediate offset.
+template <typename Tin, int DK, int DV, int RG>
+__global__ void __launch_bounds__((DV < 32 ? 32 : DV) * RG)
+    kda_decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+                      const Tin* __restrict__ v, const Tin* __restrict__ theta,
+                      const Tin* __restrict__ beta, float g_min, float* __restrict__ state,
+                      float* __restrict__ out) {
+  constexpr int DVT = DV < 32 ? 32 : DV;  // threads per row group
+  constexpr int R = DK / RG;              // rows per thread
+  __shared__ float sk[DK], sq[DK], se[DK];
+  __shared__ float red[2][RG][DVT];
+  const int64_t head = blockIdx.x;  // sequence * H + head
+  const int tid = threadIdx.x, j = tid % DVT, rg = tid / DVT;
+  for (int i = tid; i < DK; i += DVT * RG) {
+    const float th = to_f32(theta[head * DK + i]);
+    se[i] = expf(g_min * (1.0f / (1.0f + expf(-th))));
+    sk[i] = to_f32(k[head * DK + i]);
+    sq[i] = to_f32(q[head * DK + i]);
+  }
+  __syncthreads();
+  const bool active = j < DV;
+  float* col = state + head * DK * DV + (int64_t)rg * R * DV + j;
+  float s[R];
+  float ks = 0.0f;
+  if (active) {
+#pragma unroll
+    for (int i = 0; i < R; ++i) s[i] = col[i * DV];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      s[i] *= se[rg * R + i];
+      ks = fmaf(sk[rg * R + i], s[i], ks);
+    }
+  }
+  red[0][rg][j] = ks;
+  __syncthreads();
+  float kts = 0.0f;
+#pragma unroll
+  for (int r = 0; r < RG; ++r) kts += red[0][r][j];
+  float o = 0.0f;
+  if (active) {
+    const float u = to_f32(beta[head]) * (to_f32(v[head * DV + j]) - kts);
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      s[i] = fmaf(sk[rg * R + i], u, s[i]);
+      o = fmaf(sq[rg * R + i], s[i], o);
+      col[i * DV] = s[i];
+    }
+  }
+  red[1][rg][j] = o;
+  __syncthreads();
+  if (rg == 0 && active) {
+    float ot = 0.0f;
+#pragma unroll
+    for (int r = 0; r < RG; ++r) ot += red[1][r][j];
+    out[head * DV + j] = ot;
+  }
+}
+
+template <typename Tin, int DK, int DV>
+void launch_decode_kv(const DecodeParams& p, unsigned blocks, cudaStream_t stream) {
+  constexpr int RG = DK > 64 ? DK / 64 : 1;  // at most 64 rows per thread
+  constexpr int DVT = DV < 32 ? 32 : DV;
+  kda_decode_kernel<Tin, DK, DV, RG><<<blocks, DVT * RG, 0, stream>>>(
+      (const Tin*)p.q, (const Tin*)p.k, (const Tin*)p.v, (const Tin*)p.theta, (const Tin*)p.beta,
+      p.g_min, p.state, p.out);
+}
+
+template <typename Tin, int DK>
+int launch_decode_k(const DecodeParams& p, unsigned blocks, cudaStream_t stream) {
+  switch (p.dv) {
+    case 16: launch_decode_kv<Tin, DK, 16>(p, blocks, stream); break;
+    case 32: launch_decode_kv<Tin, DK, 32>(p, blocks, stream); break;
+    case 64: launch_decode_kv<Tin, DK, 64>(p, blocks, stream); break;
+    case 128: launch_decode_kv<Tin, DK, 128>(p, blocks, stream); break;
+    default: return KDA_ERR_UNSUPPORTED_SHAPE;
+  }
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+}
+
+template <typename Tin>
+int launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
+  const unsigned blocks = (unsigned)((int64_t)p.N * p.H);
+  switch (p.dk) {
+    case 16: return launch_decode_k<Tin, 16>(p, blocks, stream);
+    case 32: return launch_decode_k<Tin, 32>(p, blocks, stream);
+    case 64: return launch_decode_k<Tin, 64>(p, blocks, stream);
+    case 128: return launch_decode_k<Tin, 128>(p, blocks, stream);
+    default: return KDA_ERR_UNSUPPORTED_SHAPE;
+  }
+}
+
+}  // namespace
+
+int launch_decode(const DecodeParams& p, cudaStream_t stream) {
+  if (p.N == 0) return KDA_OK;
+  if (p.dtype == KDA_DTYPE_F32) return launch_decode_t<float>(p, stream);
+  return launch_decode_t<__nv_bfloat16>(p, stream);
+}
+
+}  // namespace kda

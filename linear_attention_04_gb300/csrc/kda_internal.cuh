@@ -32,6 +32,22 @@ struct FwdParams {
   int out_dtype;              // KDA_DTYPE_* of out
 };
 
+// Validated parameters of one decode step (one token per sequence and head).
+struct DecodeParams {
+  const void* q;      // [N, H, dk]
+  const void* k;      // [N, H, dk]
+  const void* v;      // [N, H, dv]
+  const void* theta;  // [N, H, dk]
+  const void* beta;   // [N, H]
+  float g_min;
+  float* state;       // [N, H, dk, dv] fp32, read and overwritten
+  float* out;         // [N, H, dv] fp32
+  int N, H, dk, dv;
+  int dtype;          // KDA_DTYPE_* of q, k, v, theta, beta
+};
+
+int launch_decode(const DecodeParams& p, cudaStream_t stream);
+
 // Device status word of the current device (bounded waits write it).
 int* status_word_device_ptr();
 

@@ -69,6 +69,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                 fn = getattr(lib, name)
                 fn.restype = i
                 fn.argtypes = sig
+            lib.kda_decode_step.restype = i
+            lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp]
             lib.kda_chunk_fwd_ex.restype = i
             lib.kda_chunk_fwd_ex.argtypes = [ctypes.POINTER(_Args), vp]
             lib.kda_device_status.restype = i
@@ -156,6 +158,44 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torc
     if rc != KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd_ex")
     return out, final_state
+
+
+def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torch.Tensor,
+                    beta: torch.Tensor, state: torch.Tensor, g_min: float = -5.0,
+                    out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One recurrent step through the C ABI (``kda_decode_step``): q, k, theta
+    [N,H,dk]; v [N,H,dv]; beta [N,H] (all bf16 or all fp32, contiguous, on one
+    CUDA device); state fp32 [N,H,dk,dv] is updated in place.  Returns out fp32
+    [N,H,dv].  Asynchronous on ``stream``."""
+    lib = load()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype = q.dtype
+    if dtype not in DTYPES:
+        raise TypeError(f"unsupported dtype {dtype}")
+    for name, t, shape in (("k", k, (N, H, dk)), ("theta", theta, (N, H, dk)),
+                           ("v", v, (N, H, dv)), ("beta", beta, (N, H))):
+        if t.dtype != dtype or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name}: expected contiguous {dtype} {shape}, got {t.dtype} "
+                             f"{tuple(t.shape)}")
+        if t.device != q.device:
+            raise ValueError(f"{name} on {t.device}, q on {q.device}")
+    if not q.is_cuda or not q.is_contiguous():
+        raise ValueError("q must be a contiguous CUDA tensor")
+    if state.dtype != torch.float32 or tuple(state.shape) != (N, H, dk, dv) or \
+            not state.is_contiguous() or state.device != q.device:
+        raise ValueError(f"state: expected contiguous fp32 {(N, H, dk, dv)} on {q.device}")
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=torch.float32, device=q.device)
+    elif out.dtype != torch.float32 or tuple(out.shape) != (N, H, dv) or not out.is_contiguous():
+        raise ValueError(f"out: expected contiguous fp32 {(N, H, dv)}")
+    with torch.cuda.device(q.device):
+        rc = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(theta), _ptr(beta), float(g_min),
+                                 _ptr(state), _ptr(out), N, H, dk, dv, DTYPES[dtype],
+                                 _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_step")
+    return out
 
 
 def kda_device_status(clear: bool = False) -> int:

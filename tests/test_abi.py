@@ -84,3 +84,35 @@ def test_select_path_host_logic():
     assert lib.kda_select_path(5, 128, 128) == binding.KDA_ERR_INVALID_ARG
     assert lib.kda_select_path(0, 64, 64) == 1          # bf16 off the 128 x 128 shape -> SIMT
     assert lib.kda_select_path(0, 128, 128) == 3        # bf16, dk = dv = 128 -> register-resident path
+
+
+def _decode(lib, **over):
+    a = dict(q=0x1000, k=0x2000, v=0x3000, theta=0x4000, beta=0x5000, g_min=-5.0, state=0x6000,
+             out=0x7000, N=2, H=4, dk=128, dv=128, dtype=0)
+    a.update(over)
+    return lib.kda_decode_step(a["q"], a["k"], a["v"], a["theta"], a["beta"], a["g_min"],
+                               a["state"], a["out"], a["N"], a["H"], a["dk"], a["dv"], a["dtype"],
+                               None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(state=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(out=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(N=-1), binding.KDA_ERR_INVALID_ARG),
+    (dict(H=0), binding.KDA_ERR_INVALID_ARG),
+    (dict(g_min=0.0), binding.KDA_ERR_INVALID_ARG),
+    (dict(dtype=4), binding.KDA_ERR_INVALID_ARG),
+    (dict(dk=48), binding.KDA_ERR_UNSUPPORTED_SHAPE),
+    (dict(dv=8), binding.KDA_ERR_UNSUPPORTED_SHAPE),
+    (dict(theta=0x4008), binding.KDA_ERR_MISALIGNED),
+    (dict(state=0x6004), binding.KDA_ERR_MISALIGNED),
+])
+def test_decode_host_side_rejection(over, code):
+    assert _decode(binding.load(), **over) == code
+
+
+def test_decode_empty_batch_is_a_noop():
+    # N = 0 returns before any device work (null pointers allowed)
+    assert _decode(binding.load(), N=0, q=None, k=None, v=None, theta=None, beta=None, state=None,
+                   out=None) == binding.KDA_OK
