@@ -283,8 +283,19 @@ def run_ours(args, rank, world, local):
     fin = torch.empty((inp["N"], w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    ws = None
+    if args.segments > 1:
+        from linear_attention_04_gb300 import kda_chunk_fwd_segmented, kda_segmented_workspace_size
+        ws = torch.empty(kda_segmented_workspace_size(w.B, w.H, w.T, w.dk, w.dv, args.segments),
+                         dtype=torch.uint8, device=dev)
+        path = f"segmented x{args.segments} (mma)"
+
     def step():
-        kda_chunk_fwd(q, k, v, th, be, w.g_min, init, out, fin, cu, path=path, stream=stream)
+        if ws is not None:
+            kda_chunk_fwd_segmented(q, k, v, th, be, w.g_min, init, out, fin,
+                                    segments=args.segments, workspace=ws, stream=stream)
+        else:
+            kda_chunk_fwd(q, k, v, th, be, w.g_min, init, out, fin, cu, path=path, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -334,6 +345,8 @@ def run_ours(args, rank, world, local):
     flops = chunk_gemm_flops(w, inp)
     achieved = alg / avg_launch_s / 1e9
     kname = {"tc": "kda_fwd_tc_kernel", "mma": "kda_fwd_mma_kernel"}.get(path, "kda_fwd_simt_kernel")
+    if ws is not None:
+        kname = "kda_fwd_mma_kernel"
     traffic, traffic_src = traffic_from_profiles(kname, w.name)
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -364,8 +377,12 @@ def run_ours(args, rank, world, local):
                 d.copy_(h, non_blocking=True)
             if dinit is not None:
                 dinit.copy_(hinit, non_blocking=True)
-            kda_chunk_fwd(dq, dk_, dv_, dth, dbe, w.g_min, dinit, out, fin, cu, path=path,
-                          stream=stream)
+            if ws is not None:
+                kda_chunk_fwd_segmented(dq, dk_, dv_, dth, dbe, w.g_min, dinit, out, fin,
+                                        segments=args.segments, workspace=ws, stream=stream)
+            else:
+                kda_chunk_fwd(dq, dk_, dv_, dth, dbe, w.g_min, dinit, out, fin, cu, path=path,
+                              stream=stream)
             hout.copy_(out, non_blocking=True)
             hfin.copy_(fin, non_blocking=True)
 
@@ -539,6 +556,8 @@ def main(argv=None):
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--segments", type=int, default=1,
+                    help="fwd: cut each sequence into this many segments (segment-parallel path)")
     ap.add_argument("--op", choices=["fwd", "decode"], default="fwd",
                     help="fwd: the chunked forward (the headline); decode: one recurrent step")
     args = ap.parse_args(argv)

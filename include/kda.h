@@ -142,6 +142,30 @@ typedef struct kda_fwd_args {
 KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* args, cudaStream_t stream);
 
 /*
+ * kda_chunk_fwd_segmented -- the operation of kda_chunk_fwd_ex, cut along the
+ * sequence for batches with fewer (sequence, head) chains than SMs (a few
+ * very long sequences).  The recurrence is affine in the state, so over any
+ * segment S_end = Phi S_start + S_loc, with S_loc the end state from a zero
+ * start and Phi (dk x dk) the end state with v = 0 from the identity; each
+ * chain is cut into `segments` pieces of whole 16-token chunks, the pieces'
+ * (Phi, S_loc) are computed in parallel, chained in fp32, and every piece is
+ * then run from its start state.  Work grows by about (2P - 3) / P for P
+ * segments and runs on otherwise idle SMs.  Same arithmetic as the
+ * register-resident path (results equal up to rounding order).
+ * Requires bf16 inputs, dk = dv = 128 and a fixed-length batch (cu_seqlens
+ * NULL; else KDA_ERR_UNSUPPORTED_SHAPE / KDA_ERR_INVALID_ARG); args->path is
+ * ignored.  segments = 1 runs the plain path.
+ * `workspace`: device memory of at least kda_segmented_workspace_size(B, H, T,
+ * dk, dv, segments) bytes, 256-byte aligned, owned by the caller, contents
+ * need not be initialised; it is scratch until the stream has passed this
+ * call, so calls that may overlap must not share one.  The library allocates
+ * nothing.  Returns KDA_OK or KDA_ERR_*.
+ */
+KDA_API size_t kda_segmented_workspace_size(int B, int H, int T, int dk, int dv, int segments);
+KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* args, int segments, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * kda_decode_step -- one recurrent step per (sequence, head): a single new
  * token against a resident fp32 state, which is updated in place.  The same
  * recurrence as kda_chunk_fwd for T = 1 ("Kimi K3 Deep Dive", section "Core

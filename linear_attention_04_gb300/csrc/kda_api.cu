@@ -147,6 +147,49 @@ KDA_API int kda_chunk_fwd_f32(const float* q, const float* k, const float* v, co
   return kda_chunk_fwd_ex(&a, stream);
 }
 
+KDA_API size_t kda_segmented_workspace_size(int B, int H, int T, int dk, int dv, int segments) {
+  if (B <= 0 || H <= 0 || T < 0 || dk != 128 || dv != 128 || segments < 1) return 0;
+  return kda::segmented_workspace_size(B, H, T, segments);
+}
+
+KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* a, int segments, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream) {
+  int rc = kda::validate(a);
+  if (rc != KDA_OK) return rc;
+  if (a->dtype != KDA_DTYPE_BF16 || a->dk != 128 || a->dv != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+  if (a->cu_seqlens || segments < 1) return KDA_ERR_INVALID_ARG;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return KDA_ERR_MISALIGNED;
+  if (segments > 1 && a->T > 0 &&
+      (!workspace || workspace_bytes < kda::segmented_workspace_size(a->B, a->H, a->T, segments)))
+    return KDA_ERR_INVALID_ARG;
+  if (a->T == 0) {
+    kda_fwd_args b = *a;
+    b.path = KDA_PATH_MMA;
+    return kda_chunk_fwd_ex(&b, stream);
+  }
+  rc = kda::check_device();
+  if (rc != KDA_OK) return rc;
+  kda::FwdParams p;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.theta = a->theta;
+  p.beta = a->beta;
+  p.g_min = a->g_min;
+  p.init_state = a->init_state;
+  p.out = a->out;
+  p.final_state = a->final_state;
+  p.cu_seqlens = nullptr;
+  p.N = a->B;
+  p.H = a->H;
+  p.T = a->T;
+  p.dk = a->dk;
+  p.dv = a->dv;
+  p.dtype = a->dtype;
+  p.out_dtype = a->out_dtype;
+  return kda::launch_segmented(p, segments, workspace, workspace_bytes, stream);
+}
+
 KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const void* theta,
                             const void* beta, float g_min, float* state, float* out, int N, int H,
                             int dk, int dv, int dtype, cudaStream_t stream) {

@@ -55,6 +55,27 @@ int launch_simt(const FwdParams& p, cudaStream_t stream);
 int launch_tc(const FwdParams& p, cudaStream_t stream);
 bool tc_supported(int dtype, int dk, int dv);
 int launch_mma(const FwdParams& p, cudaStream_t stream);
+
+// One CTA of a segmented launch of the register-resident kernel: a token range
+// of one head, with its own initial/final state and options.
+constexpr int kJobZeroV = 1;          // V is taken as zero (the state's linear part)
+constexpr int kJobNoOut = 2;          // no output stores
+constexpr int kJobIdentityInit = 4;   // initial state = identity (dk = dv), init ignored
+struct SegJob {
+  int64_t t0, t1;          // token rows [t0, t1) of the packed [tokens, H, .] tensors
+  int head;
+  int flags;               // kJob* bits
+  const float* init;       // [dk][dv] initial state, or null (zero / identity)
+  float* final_state;      // [dk][dv] end state, or null
+};
+// Launches one CTA per job over the packed token axis (p.T = total tokens).
+int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStream_t stream);
+
+// Segment-parallel forward (fixed-length batches, bf16, dk = dv = 128): the
+// scratch it needs and the launch sequence over a caller-provided workspace.
+size_t segmented_workspace_size(int B, int H, int T, int segments);
+int launch_segmented(const FwdParams& p, int segments, void* ws, size_t ws_bytes,
+                     cudaStream_t stream);
 bool mma_supported(int dtype, int dk, int dv);
 
 // TMA map over a [tokens][H][128] bf16 tensor whose boxes are one chunk of 16

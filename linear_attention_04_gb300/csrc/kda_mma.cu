@@ -103,7 +103,7 @@ constexpr int B_FULL = 0;                     // [kIntraWarps] TMA -> intra warp
 constexpr int B_READY = kIntraWarps;          // [NSLOT] intra warp -> state warps
 constexpr int B_FREE = kIntraWarps + NSLOT;   // [NSLOT] state warps (4 arrivals) -> intra warp
 constexpr int NBARS = kIntraWarps + 2 * NSLOT;
-constexpr uint32_t SM_MISC = SM_BARS + NBARS * 8;  // abort flag
+constexpr uint32_t SM_MISC = SM_BARS + NBARS * 8;  // abort flag (+4: job flags)
 constexpr uint32_t SM_RANK = SM_MISC + 16;         // chain-order scratch
 constexpr uint32_t SM_TOTAL = SM_RANK + (kMaxRankedSeqsDev + 1) * 4;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 128;    // + alignment slack
@@ -144,6 +144,7 @@ __device__ __forceinline__ void set_regs() {
 }
 
 struct MmaArgs {
+  const SegJob* jobs;  // per-CTA work units (segmented launches), or null
   const __nv_bfloat16* beta;
   float g_min;
   const float* init_state;
@@ -197,8 +198,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ldmatrix.x4 (mi: which 8x8 matrix this lane addresses, rr: its row)
   const int g = lane >> 2, q = lane & 3, mi = lane >> 3, rr = lane & 7;
 
-  const Chain ch = chain_for_block(blockIdx.x, args.H, args.N, args.T, args.cu_seqlens,
-                                   (int*)(sm + SM_RANK));
+  // the work unit: a whole (sequence, head) chain, or one segment job
+  Chain ch;
+  int flags = 0;
+  const float* init_state = args.init_state;
+  float* final_state = args.final_state;
+  int64_t soff = 0;  // element offset of this chain's state in init/final
+  if (args.jobs) {
+    const SegJob jb = args.jobs[blockIdx.x];
+    ch.seq = 0;
+    ch.head = jb.head;
+    ch.t0 = jb.t0;
+    ch.t1 = jb.t1;
+    flags = jb.flags;
+    init_state = jb.init;
+    final_state = jb.final_state;
+  } else {
+    ch = chain_for_block(blockIdx.x, args.H, args.N, args.T, args.cu_seqlens, (int*)(sm + SM_RANK));
+    soff = ((int64_t)ch.seq * args.H + ch.head) * D * D;
+  }
+  // options read back from shared memory where they are used (keeps them out
+  // of the register budget of the main loops)
+  volatile int* sflags = (volatile int*)(sm + SM_MISC + 4);
   const int h = ch.head;
   const int H = args.H;
   const int L = (int)(ch.t1 - ch.t0);
@@ -207,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < NBARS; ++i) mbar_init(&bars[i], (i >= B_FREE) ? kStateWarps : 1);
     *abort = 0;
+    *sflags = flags;
     fence_mbar_init();
   }
   __syncthreads();
@@ -221,13 +243,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* kh = sm + SM_KH + iw * TILE;
     float* ab = (float*)(sm + SM_AB + iw * AB_BYTES);
     uint64_t* full = &bars[B_FULL + iw];
+    const bool zero_v = *sflags & kJobZeroV;
     auto load = [&](int m) {
-      mbar_arrive_expect_tx(full, STAGE);
+      mbar_arrive_expect_tx(full, zero_v ? 3 * TILE : STAGE);
       const int row = (int)(ch.t0 + (int64_t)m * C);
       tma_load_3d(st + 0 * TILE, &tm_q, 0, h, row, full);
       tma_load_3d(st + 1 * TILE, &tm_k, 0, h, row, full);
       tma_load_3d(st + 2 * TILE, &tm_th, 0, h, row, full);
-      tma_load_3d(st + 3 * TILE, &tm_v, 0, h, row, full);
+      if (!zero_v) tma_load_3d(st + 3 * TILE, &tm_v, 0, h, row, full);
     };
     int issued = 0, consumed = 0;
     if (lane == 0 && iw < nchunks) {
@@ -328,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 8; ++i) {
         const int e = lane + 32 * i, row = e >> 4, c16 = e & 15;
         *(uint4*)(sl + SL_V + row * 256 + (((c16 ^ row) & 7) | (c16 & 8)) * 16) =
-            *(const uint4*)(st + 3 * TILE + row * 256 + c16 * 16);
+            zero_v ? make_uint4(0u, 0u, 0u, 0u) : *(const uint4*)(st + 3 * TILE + row * 256 + c16 * 16);
       }
       // q_t . k_t: transpose-reduce the 16 per-lane partial sums over the warp;
       // lane l ends with token (l >> 1) & 15
@@ -461,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ state warps
     if constexpr (kStateRegs > 0) set_regs<kStateRegs>();
     const int sw = warp;
-    const int64_t soff = ((int64_t)ch.seq * H + h) * D * D;
+    const bool identity = flags & kJobIdentityInit;
     // S[m][nt][c]: S^T element (value channel 32 sw + 16 m + g + 8 (c >> 1),
     // key channel 8 nt + 2 q + (c & 1)) -- the m16n8 accumulator layout
     float S[kMT][D / 8][4];
@@ -472,7 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int dv = kDvPerWarp * sw + 16 * m + g + 8 * (c >> 1), dk = 8 * nt + 2 * q + (c & 1);
-          S[m][nt][c] = args.init_state ? args.init_state[soff + (int64_t)dk * D + dv] : 0.0f;
+          S[m][nt][c] = init_state ? init_state[soff + (int64_t)dk * D + dv]
+                                   : (identity && dk == dv ? 1.0f : 0.0f);
         }
     bool bad = false;
     for (int n = 0; n < nchunks; ++n) {
@@ -599,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const float* dc = (const float*)(sl + SL_DC);
         const float2 dc0 = *(const float2*)(dc + 2 * q), dc1 = *(const float2*)(dc + 8 + 2 * q);
-        const int nvalid = min(C, L - n * C);
+        const int nvalid = (*sflags & kJobNoOut) ? 0 : min(C, L - n * C);
         const int64_t row0 = ch.t0 + (int64_t)n * C;
 #pragma unroll
         for (int m = 0; m < kMT; ++m)
@@ -626,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid == 0) KTRACE(n, 4);
     }
     if (bad) fail(abort, args.status);
-    if (!bad && args.final_state) {
+    if (!bad && final_state) {
 #pragma unroll
       for (int m = 0; m < kMT; ++m)
 #pragma unroll
@@ -634,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int dv = kDvPerWarp * sw + 16 * m + g + 8 * (c >> 1), dk = 8 * nt + 2 * q + (c & 1);
-            args.final_state[soff + (int64_t)dk * D + dv] = S[m][nt][c];
+            final_state[soff + (int64_t)dk * D + dv] = S[m][nt][c];
           }
     }
   }
@@ -646,7 +670,7 @@ bool mma_supported(int dtype, int dk, int dv) {
   return dtype == KDA_DTYPE_BF16 && dk == D && dv == D;
 }
 
-int launch_mma(const FwdParams& p, cudaStream_t stream) {
+int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStream_t stream) {
   if (!mma_supported(p.dtype, p.dk, p.dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
   const int64_t tokens = p.cu_seqlens ? (int64_t)p.T : (int64_t)p.N * p.T;
   if (tokens <= 0) {
@@ -678,6 +702,7 @@ int launch_mma(const FwdParams& p, cudaStream_t stream) {
   });
   if (attr_err != cudaSuccess) return KDA_ERR_LAUNCH;
   MmaArgs a;
+  a.jobs = jobs;
   a.beta = (const __nv_bfloat16*)p.beta;
   a.g_min = p.g_min;
   a.init_state = p.init_state;
@@ -690,12 +715,16 @@ int launch_mma(const FwdParams& p, cudaStream_t stream) {
   a.T = p.T;
   a.status = status_word_device_ptr();
   if (!a.status) return KDA_ERR_CUDA;
+  const unsigned grid = jobs ? (unsigned)njobs : (unsigned)(p.N * p.H);
+  if (grid == 0) return KDA_OK;
   if (a.out_bf16)
-    kda_fwd_mma_kernel<true><<<(unsigned)(p.N * p.H), kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
+    kda_fwd_mma_kernel<true><<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
   else
-    kda_fwd_mma_kernel<false><<<(unsigned)(p.N * p.H), kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
+    kda_fwd_mma_kernel<false><<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
+
+int launch_mma(const FwdParams& p, cudaStream_t stream) { return launch_mma_jobs(p, nullptr, 0, stream); }
 
 }  // namespace kda
 

@@ -1,0 +1,167 @@
+// kda_segment.cu -- segment-parallel forward pass for batches of few, long
+// sequences (more SMs than (sequence, head) chains).
+//
+// The recurrence S_t = (I - b_t k_t k_t^T) Diag(e^{g_t}) S_{t-1} + b_t k_t v_t^T
+// ("Kimi K3 Deep Dive", section "Core Innovation 1") is affine in the state, so
+// over any token segment s
+//
+//     S_end = Phi_s S_start + S_loc_s,
+//
+// where S_loc_s is the end state of the segment run from a zero state and
+// Phi_s (dk x dk) the end state of the segment run with v = 0 from the
+// identity (column independence makes the identity's columns the basis of the
+// linear part).  Each chain is cut into P segments of whole 16-token chunks:
+//
+//   launch 1 (one CTA per job): segment 0 in full from the caller's initial
+//            state (outputs, end state = start of segment 1); segments
+//            1 .. P-2 from zero without outputs (S_loc); the same segments
+//            with v = 0 from the identity without outputs (Phi);
+//   combine: S_start(s + 1) = Phi_s S_start(s) + S_loc_s, s = 1 .. P-2 (fp32);
+//   launch 2: segments 1 .. P-1 in full from their start states (outputs; the
+//            last one writes the caller's final state).
+//
+// Work per chain grows by about (2P - 3) / P segment-lengths, run in parallel
+// on otherwise idle SMs.  All scratch lives in a caller-provided workspace
+// (kda_segmented_workspace_size).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int D = 128;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct SegPlan {
+  int P;           // segments per chain (effective)
+  int64_t Ltok;    // tokens per segment (whole chunks; the last may be shorter)
+  int64_t NH;      // chains
+  size_t off_jobs1, off_jobs2, off_sst, off_sloc, off_phi, total;
+};
+
+SegPlan plan(int B, int H, int T, int segments) {
+  SegPlan s;
+  const int64_t nchunks = ((int64_t)T + kChunk - 1) / kChunk;
+  int P = segments < 1 ? 1 : segments;
+  if (P > nchunks) P = (int)(nchunks > 0 ? nchunks : 1);
+  const int64_t per = (nchunks + P - 1) / P;  // chunks per segment
+  P = (int)((nchunks + per - 1) / per);       // no empty segment
+  s.P = P;
+  s.Ltok = per * kChunk;
+  s.NH = (int64_t)B * H;
+  const int64_t n1 = s.NH * (P >= 2 ? 2 * P - 3 : 0);
+  const int64_t n2 = s.NH * (P - 1);
+  const size_t st = (size_t)D * D * sizeof(float);
+  s.off_jobs1 = 0;
+  s.off_jobs2 = align_up(s.off_jobs1 + (size_t)n1 * sizeof(SegJob));
+  s.off_sst = align_up(s.off_jobs2 + (size_t)n2 * sizeof(SegJob));
+  s.off_sloc = align_up(s.off_sst + (size_t)(s.NH * (P - 1)) * st);
+  s.off_phi = align_up(s.off_sloc + (size_t)(s.NH * (P > 2 ? P - 2 : 0)) * st);
+  s.total = align_up(s.off_phi + (size_t)(s.NH * (P > 2 ? P - 2 : 0)) * st);
+  return s;
+}
+
+// Fills both job tables (one thread per chain).
+__global__ void seg_setup_kernel(SegJob* jobs1, SegJob* jobs2, float* sst, float* sloc, float* phi,
+                                 const float* init, float* fin, int64_t NH, int H, int64_t T,
+                                 int P, int64_t Ltok) {
+  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= NH) return;
+  const int64_t b = c / H;
+  const int h = (int)(c - b * H);
+  const int64_t base = b * T;
+  const size_t st = (size_t)D * D;
+  auto seg = [&](int s, SegJob& j) {
+    j.t0 = base + (int64_t)s * Ltok;
+    j.t1 = base + ((int64_t)(s + 1) * Ltok < T ? (int64_t)(s + 1) * Ltok : T);
+    j.head = h;
+  };
+  // launch 1: segment 0 in full; segments 1 .. P-2 local and transition
+  SegJob j;
+  seg(0, j);
+  j.flags = 0;
+  j.init = init ? init + c * st : nullptr;
+  j.final_state = sst + (size_t)(c * (P - 1)) * st;
+  jobs1[c] = j;
+  for (int s = 1; s <= P - 2; ++s) {
+    seg(s, j);
+    j.flags = kJobNoOut;
+    j.init = nullptr;
+    j.final_state = sloc + (size_t)(c * (P - 2) + (s - 1)) * st;
+    jobs1[NH * s + c] = j;
+    j.flags = kJobZeroV | kJobNoOut | kJobIdentityInit;
+    j.final_state = phi + (size_t)(c * (P - 2) + (s - 1)) * st;
+    jobs1[NH * (P - 1 + s - 1) + c] = j;
+  }
+  // launch 2: segments 1 .. P-1 in full from their start states
+  for (int s = 1; s <= P - 1; ++s) {
+    seg(s, j);
+    j.flags = 0;
+    j.init = sst + (size_t)(c * (P - 1) + (s - 1)) * st;
+    j.final_state = (s == P - 1 && fin) ? fin + c * st : nullptr;
+    jobs2[NH * (s - 1) + c] = j;
+  }
+}
+
+// S_start(s + 1) = Phi_s S_start(s) + S_loc_s for every chain, in fp32: block
+// (chain, 16-row tile), thread = value column.
+__global__ void __launch_bounds__(D) seg_combine_kernel(float* sst, const float* sloc, const float* phi,
+                                                         int P, int s) {
+  const int64_t c = blockIdx.x;
+  const int i0 = blockIdx.y * 16, j = threadIdx.x;
+  const size_t st = (size_t)D * D;
+  const float* prev = sst + (size_t)(c * (P - 1) + (s - 1)) * st;
+  const float* ph = phi + (size_t)(c * (P - 2) + (s - 1)) * st;
+  const float* lo = sloc + (size_t)(c * (P - 2) + (s - 1)) * st;
+  float* nxt = sst + (size_t)(c * (P - 1) + s) * st;
+  float acc[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) acc[r] = lo[(size_t)(i0 + r) * D + j];
+  for (int kk = 0; kk < D; ++kk) {
+    const float p = prev[(size_t)kk * D + j];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) acc[r] = fmaf(ph[(size_t)(i0 + r) * D + kk], p, acc[r]);
+  }
+#pragma unroll
+  for (int r = 0; r < 16; ++r) nxt[(size_t)(i0 + r) * D + j] = acc[r];
+}
+
+}  // namespace
+
+size_t segmented_workspace_size(int B, int H, int T, int segments) {
+  return plan(B, H, T, segments).total;
+}
+
+int launch_segmented(const FwdParams& p, int segments, void* ws, size_t ws_bytes,
+                     cudaStream_t stream) {
+  const SegPlan pl = plan(p.N, p.H, p.T, segments);
+  if (pl.P < 2) return launch_mma(p, stream);
+  if (!ws || ws_bytes < pl.total) return KDA_ERR_INVALID_ARG;
+  unsigned char* w = (unsigned char*)ws;
+  SegJob* jobs1 = (SegJob*)(w + pl.off_jobs1);
+  SegJob* jobs2 = (SegJob*)(w + pl.off_jobs2);
+  float* sst = (float*)(w + pl.off_sst);
+  float* sloc = (float*)(w + pl.off_sloc);
+  float* phi = (float*)(w + pl.off_phi);
+  seg_setup_kernel<<<(unsigned)((pl.NH + 127) / 128), 128, 0, stream>>>(
+      jobs1, jobs2, sst, sloc, phi, p.init_state, p.final_state, pl.NH, p.H, p.T, pl.P, pl.Ltok);
+  if (cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
+  // the kernels see the batch as one packed sequence of B * T tokens
+  FwdParams q = p;
+  q.T = (int)((int64_t)p.N * p.T);
+  q.N = 1;
+  q.cu_seqlens = nullptr;
+  int rc = launch_mma_jobs(q, jobs1, (int)(pl.NH * (2 * pl.P - 3)), stream);
+  if (rc != KDA_OK) return rc;
+  for (int s = 1; s <= pl.P - 2; ++s) {
+    seg_combine_kernel<<<dim3((unsigned)pl.NH, D / 16), D, 0, stream>>>(sst, sloc, phi, pl.P, s);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
+  }
+  return launch_mma_jobs(q, jobs2, (int)(pl.NH * (pl.P - 1)), stream);
+}
+
+}  // namespace kda

@@ -69,6 +69,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                 fn = getattr(lib, name)
                 fn.restype = i
                 fn.argtypes = sig
+            lib.kda_segmented_workspace_size.restype = ctypes.c_size_t
+            lib.kda_segmented_workspace_size.argtypes = [i, i, i, i, i, i]
+            lib.kda_chunk_fwd_segmented.restype = i
+            lib.kda_chunk_fwd_segmented.argtypes = [ctypes.POINTER(_Args), i, vp, ctypes.c_size_t,
+                                                    vp]
             lib.kda_decode_step.restype = i
             lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp]
             lib.kda_chunk_fwd_ex.restype = i
@@ -157,6 +162,52 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torc
         rc = lib.kda_chunk_fwd_ex(ctypes.byref(a), _stream_ptr(stream))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd_ex")
+    return out, final_state
+
+
+def kda_segmented_workspace_size(B: int, H: int, T: int, dk: int, dv: int, segments: int) -> int:
+    return int(load().kda_segmented_workspace_size(B, H, T, dk, dv, segments))
+
+
+def kda_chunk_fwd_segmented(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                            theta: torch.Tensor, beta: torch.Tensor, g_min: float = -5.0,
+                            init_state: Optional[torch.Tensor] = None,
+                            out: Optional[torch.Tensor] = None,
+                            final_state: Optional[torch.Tensor] = None, *, segments: int = 4,
+                            workspace: Optional[torch.Tensor] = None,
+                            want_final_state: bool = True, out_dtype: torch.dtype = torch.float32,
+                            stream=None):
+    """Segment-parallel forward through the C ABI (``kda_chunk_fwd_segmented``):
+    same arguments and results as ``kda_chunk_fwd`` for a fixed-length bf16
+    batch with dk = dv = 128.  ``workspace`` is a uint8 CUDA tensor of at least
+    ``kda_segmented_workspace_size`` bytes (allocated here when not given)."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for name, t, shape in (("k", k, (B, T, H, dk)), ("theta", theta, (B, T, H, dk)),
+                           ("v", v, (B, T, H, dv)), ("beta", beta, (B, T, H))):
+        if t.dtype != q.dtype or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name}: expected contiguous {q.dtype} {shape}")
+    sshape = (B, H, dk, dv)
+    if init_state is not None and (init_state.dtype != torch.float32 or
+                                   tuple(init_state.shape) != sshape or
+                                   not init_state.is_contiguous()):
+        raise ValueError(f"init_state: expected contiguous fp32 {sshape}")
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=out_dtype, device=q.device)
+    if final_state is None and want_final_state:
+        final_state = torch.empty(sshape, dtype=torch.float32, device=q.device)
+    need = kda_segmented_workspace_size(B, H, T, dk, dv, segments)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    a = _Args(_ptr(q), _ptr(k), _ptr(v), _ptr(theta), _ptr(beta), float(g_min),
+              _ptr(init_state), _ptr(out), _ptr(final_state), None, B, H, T, dk, dv,
+              DTYPES[q.dtype], DTYPES[out_dtype], PATHS["mma"])
+    with torch.cuda.device(q.device):
+        rc = lib.kda_chunk_fwd_segmented(ctypes.byref(a), int(segments), _ptr(workspace),
+                                         workspace.numel(), _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd_segmented")
     return out, final_state
 
 

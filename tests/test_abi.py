@@ -116,3 +116,33 @@ def test_decode_empty_batch_is_a_noop():
     # N = 0 returns before any device work (null pointers allowed)
     assert _decode(binding.load(), N=0, q=None, k=None, v=None, theta=None, beta=None, state=None,
                    out=None) == binding.KDA_OK
+
+
+def test_segmented_workspace_size_host_logic():
+    lib = binding.load()
+    n1 = lib.kda_segmented_workspace_size(1, 32, 262144, 128, 128, 4)
+    n2 = lib.kda_segmented_workspace_size(1, 32, 262144, 128, 128, 8)
+    assert 0 < n1 < n2 and n1 % 256 == 0
+    # one segment needs no scratch beyond alignment; bad shapes give 0
+    assert lib.kda_segmented_workspace_size(1, 32, 262144, 128, 128, 1) < 1024
+    assert lib.kda_segmented_workspace_size(1, 32, 4096, 64, 128, 4) == 0
+    assert lib.kda_segmented_workspace_size(0, 32, 4096, 128, 128, 4) == 0
+
+
+@pytest.mark.parametrize("over,extra,code", [
+    (dict(dtype=1), {}, binding.KDA_ERR_UNSUPPORTED_SHAPE),
+    (dict(dk=64), {}, binding.KDA_ERR_UNSUPPORTED_SHAPE),
+    (dict(cu_seqlens=0x9000), {}, binding.KDA_ERR_INVALID_ARG),
+    (dict(), dict(segments=0), binding.KDA_ERR_INVALID_ARG),
+    (dict(T=4096), dict(ws=0x10000, nbytes=64), binding.KDA_ERR_INVALID_ARG),
+    (dict(T=4096), dict(ws=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(T=4096), dict(ws=0x10010), binding.KDA_ERR_MISALIGNED),
+    (dict(q=None, T=4096), {}, binding.KDA_ERR_INVALID_ARG),
+])
+def test_segmented_host_side_rejection(over, extra, code):
+    lib = binding.load()
+    a = _args(**over)
+    seg = extra.get("segments", 4)
+    ws = extra.get("ws", 0x10000)
+    nbytes = extra.get("nbytes", 1 << 40)
+    assert lib.kda_chunk_fwd_segmented(ctypes.byref(a), seg, ws, nbytes, None) == code
