@@ -78,6 +78,7 @@ extern "C" {
 #define KDA_ERR_DEVICE_TIMEOUT (-5)     /* a bounded device wait ran out (status word)   */
 #define KDA_ERR_CUDA (-6)               /* another CUDA runtime error                    */
 #define KDA_ERR_UNSUPPORTED_SHAPE (-7)  /* dk/dv outside {16,32,64,128} for this path    */
+#define KDA_ERR_SCRATCH_TOO_SMALL (-8)  /* the fixed scratch area cannot hold the call   */
 
 /* kernel path selection for kda_chunk_fwd_ex */
 #define KDA_PATH_AUTO 0 /* KDA_PATH_MMA for bf16 with dk = dv = 128, else SIMT        */
@@ -164,6 +165,33 @@ KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* args, cudaStream_t stream);
 KDA_API size_t kda_segmented_workspace_size(int B, int H, int T, int dk, int dv, int segments);
 KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* args, int segments, void* workspace,
                                     size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of the scratch area built into the library for
+ * kda_chunk_fwd_segmented_noalloc (24 MiB per device). */
+#define KDA_NOALLOC_SCRATCH_BYTES (24u << 20)
+
+/*
+ * kda_chunk_fwd_segmented_noalloc -- kda_chunk_fwd_segmented over a scratch
+ * area that is part of the library itself, for callers that cannot provide
+ * a workspace (no allocation of any kind at call time: no cudaMalloc, no
+ * allocating library).  The pages have no counterpart of this entry point; it
+ * is an interface convenience of this library.
+ * - Limit: a call needs kda_segmented_workspace_size(B, H, T, 128, 128,
+ *   segments) bytes; above KDA_NOALLOC_SCRATCH_BYTES it returns
+ *   KDA_ERR_SCRATCH_TOO_SMALL before anything is queued (use the workspace
+ *   entry point then).  Example: B=1, H=32 fits up to segments = 5.
+ * - Nothing in the area needs to start at zero; every call writes the parts
+ *   it reads.
+ * - There is one area per device: calls on the same device whose execution
+ *   may overlap (other streams, other host threads) race on it and must be
+ *   serialised by the caller.
+ * - The area's device address is looked up once per device, by the first
+ *   call made with that device current; make that first call before any
+ *   stream capture on that device.
+ * Arguments, requirements and results otherwise as kda_chunk_fwd_segmented.
+ */
+KDA_API int kda_chunk_fwd_segmented_noalloc(const kda_fwd_args* args, int segments,
+                                            cudaStream_t stream);
 
 /*
  * kda_decode_step -- one recurrent step per (sequence, head): a single new

@@ -190,6 +190,21 @@ KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* a, int segments, void* w
   return kda::launch_segmented(p, segments, workspace, workspace_bytes, stream);
 }
 
+KDA_API int kda_chunk_fwd_segmented_noalloc(const kda_fwd_args* a, int segments,
+                                            cudaStream_t stream) {
+  int rc = kda::validate(a);
+  if (rc != KDA_OK) return rc;
+  if (a->dtype != KDA_DTYPE_BF16 || a->dk != 128 || a->dv != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+  if (a->cu_seqlens || segments < 1) return KDA_ERR_INVALID_ARG;
+  const size_t need = a->T > 0 ? kda::segmented_workspace_size(a->B, a->H, a->T, segments) : 0;
+  if (need > kda::kNoallocScratchBytes) return KDA_ERR_SCRATCH_TOO_SMALL;
+  rc = kda::check_device();
+  if (rc != KDA_OK) return rc;
+  void* scratch = kda::noalloc_scratch();
+  if (!scratch) return KDA_ERR_CUDA;
+  return kda_chunk_fwd_segmented(a, segments, scratch, kda::kNoallocScratchBytes, stream);
+}
+
 KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const void* theta,
                             const void* beta, float g_min, float* state, float* out, int N, int H,
                             int dk, int dv, int dtype, cudaStream_t stream) {
@@ -245,6 +260,7 @@ KDA_API const char* kda_strerror(int code) {
     case KDA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
     case KDA_ERR_CUDA: return "CUDA runtime error";
     case KDA_ERR_UNSUPPORTED_SHAPE: return "unsupported (dtype, dk, dv) for this kernel path";
+    case KDA_ERR_SCRATCH_TOO_SMALL: return "the library's scratch area cannot hold this call";
     default: return "unknown status code";
   }
 }

@@ -74,6 +74,11 @@ int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStrea
 // Segment-parallel forward (fixed-length batches, bf16, dk = dv = 128): the
 // scratch it needs and the launch sequence over a caller-provided workspace.
 size_t segmented_workspace_size(int B, int H, int T, int segments);
+
+// The library's own scratch area for kda_chunk_fwd_segmented_noalloc (one per
+// device, part of the library image); null if its address cannot be found.
+constexpr size_t kNoallocScratchBytes = (size_t)KDA_NOALLOC_SCRATCH_BYTES;
+void* noalloc_scratch();
 int launch_segmented(const FwdParams& p, int segments, void* ws, size_t ws_bytes,
                      cudaStream_t stream);
 bool mma_supported(int dtype, int dk, int dv);

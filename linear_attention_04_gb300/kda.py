@@ -24,6 +24,7 @@ KDA_ERR_LAUNCH = -4
 KDA_ERR_DEVICE_TIMEOUT = -5
 KDA_ERR_CUDA = -6
 KDA_ERR_UNSUPPORTED_SHAPE = -7
+KDA_ERR_SCRATCH_TOO_SMALL = -8
 
 PATHS = {"auto": 0, "simt": 1, "tc": 2, "mma": 3}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
@@ -74,6 +75,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.kda_chunk_fwd_segmented.restype = i
             lib.kda_chunk_fwd_segmented.argtypes = [ctypes.POINTER(_Args), i, vp, ctypes.c_size_t,
                                                     vp]
+            lib.kda_chunk_fwd_segmented_noalloc.restype = i
+            lib.kda_chunk_fwd_segmented_noalloc.argtypes = [ctypes.POINTER(_Args), i, vp]
             lib.kda_decode_step.restype = i
             lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp]
             lib.kda_chunk_fwd_ex.restype = i
@@ -208,6 +211,28 @@ def kda_chunk_fwd_segmented(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                          workspace.numel(), _stream_ptr(stream))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd_segmented")
+    return out, final_state
+
+
+def kda_chunk_fwd_segmented_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                                    theta: torch.Tensor, beta: torch.Tensor, g_min: float,
+                                    init_state: Optional[torch.Tensor], out: torch.Tensor,
+                                    final_state: Optional[torch.Tensor], *, segments: int = 4,
+                                    out_dtype: torch.dtype = torch.float32, stream=None):
+    """``kda_chunk_fwd_segmented_noalloc`` through the C ABI: the segment-parallel
+    forward over the library's own scratch area.  ``out`` (and ``final_state``
+    when wanted) are caller tensors; nothing is allocated here."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    a = _Args(_ptr(q), _ptr(k), _ptr(v), _ptr(theta), _ptr(beta), float(g_min),
+              _ptr(init_state), _ptr(out), _ptr(final_state), None, B, H, T, dk, dv,
+              DTYPES[q.dtype], DTYPES[out_dtype], PATHS["mma"])
+    with torch.cuda.device(q.device):
+        rc = lib.kda_chunk_fwd_segmented_noalloc(ctypes.byref(a), int(segments),
+                                                 _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd_segmented_noalloc")
     return out, final_state
 
 

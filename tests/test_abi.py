@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_strerror_and_version():
     lib = binding.load()
-    for code in range(-7, 1):
+    for code in range(-8, 1):
         assert lib.kda_strerror(code)
     assert lib.kda_strerror(-999) == b"unknown status code"
     assert lib.kda_version() >= 100
@@ -146,3 +146,24 @@ def test_segmented_host_side_rejection(over, extra, code):
     ws = extra.get("ws", 0x10000)
     nbytes = extra.get("nbytes", 1 << 40)
     assert lib.kda_chunk_fwd_segmented(ctypes.byref(a), seg, ws, nbytes, None) == code
+
+
+@pytest.mark.parametrize("over,seg,code", [
+    (dict(B=1, H=32, T=262144), 16, binding.KDA_ERR_SCRATCH_TOO_SMALL),   # needs > 24 MiB
+    (dict(B=8, H=32, T=8192), 4, binding.KDA_ERR_SCRATCH_TOO_SMALL),
+    (dict(dtype=1), 4, binding.KDA_ERR_UNSUPPORTED_SHAPE),
+    (dict(cu_seqlens=0x9000), 4, binding.KDA_ERR_INVALID_ARG),
+    (dict(), 0, binding.KDA_ERR_INVALID_ARG),
+    (dict(g_min=0.5), 4, binding.KDA_ERR_INVALID_ARG),
+])
+def test_noalloc_host_side_rejection(over, seg, code):
+    lib = binding.load()
+    a = _args(**over)
+    assert lib.kda_chunk_fwd_segmented_noalloc(ctypes.byref(a), seg, None) == code
+
+
+def test_noalloc_capacity_covers_the_long_workload():
+    lib = binding.load()
+    cap = 24 << 20
+    assert lib.kda_segmented_workspace_size(1, 32, 262144, 128, 128, 5) <= cap
+    assert lib.kda_segmented_workspace_size(1, 32, 262144, 128, 128, 6) > cap
