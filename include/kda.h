@@ -86,6 +86,10 @@ extern "C" {
 #define KDA_PATH_TC 2   /* tcgen05/TMEM tensor-core path (bf16, dk = dv = 128)         */
 #define KDA_PATH_MMA 3  /* register-resident mma.sync path (bf16, dk = dv = 128)       */
 
+/* gate parameterisation (kda_fwd_args.gate) */
+#define KDA_GATE_SIGMOID 0   /* g = g_min * sigmoid(theta): the bounded gate (default)     */
+#define KDA_GATE_LOG_DECAY 1 /* theta holds the log-decay g <= 0 itself; g_min is ignored  */
+
 /* element types of q, k, v, theta, beta and out */
 #define KDA_DTYPE_BF16 0
 #define KDA_DTYPE_F32 1
@@ -122,7 +126,15 @@ KDA_API int kda_chunk_fwd_f32(const float* q, const float* k, const float* v, co
  * theta and beta; `out_dtype` that of out (KDA_DTYPE_F32, or KDA_DTYPE_BF16
  * to halve the output bytes at the cost of bf16 rounding of o; fp32 inputs
  * require an fp32 out).  `path` is KDA_PATH_*; KDA_PATH_TC and KDA_PATH_MMA
- * require bf16 inputs and dk = dv = 128 (else KDA_ERR_UNSUPPORTED_SHAPE). */
+ * require bf16 inputs and dk = dv = 128 (else KDA_ERR_UNSUPPORTED_SHAPE).
+ * `gate` selects how theta becomes the log-decay.  KDA_GATE_SIGMOID is the
+ * bounded gate of the pages, under which every in-chunk factor e^{-G} stays
+ * at or below e^{80}.  KDA_GATE_LOG_DECAY takes g from theta as given (any
+ * g <= 0, for instance -softplus of a logit) with no bound: the tensor-core
+ * paths then need the in-chunk sum of |g| over any 16 tokens to stay below
+ * about 88 (fp32 and bf16 overflow of e^{-G}), else their results are not
+ * finite; the SIMT path has the same limit.  KDA_PATH_TC supports only
+ * KDA_GATE_SIGMOID. */
 typedef struct kda_fwd_args {
   const void* q;
   const void* k;
@@ -138,6 +150,7 @@ typedef struct kda_fwd_args {
   int dtype;
   int out_dtype;
   int path;
+  int gate; /* KDA_GATE_*; zero-initialised structs get the bounded gate */
 } kda_fwd_args;
 
 KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* args, cudaStream_t stream);

@@ -52,7 +52,9 @@ int validate(const kda_fwd_args* a) {
   // token tensors may be empty (null) only when there are no tokens
   if (a->T > 0 && (!a->q || !a->k || !a->v || !a->theta || !a->beta || !a->out))
     return KDA_ERR_INVALID_ARG;
-  if (!(a->g_min < 0.0f) || a->g_min != a->g_min) return KDA_ERR_INVALID_ARG;
+  if (a->gate != KDA_GATE_SIGMOID && a->gate != KDA_GATE_LOG_DECAY) return KDA_ERR_INVALID_ARG;
+  if (a->gate == KDA_GATE_SIGMOID && (!(a->g_min < 0.0f) || a->g_min != a->g_min))
+    return KDA_ERR_INVALID_ARG;
   if (a->dtype != KDA_DTYPE_BF16 && a->dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
   if (a->out_dtype != KDA_DTYPE_BF16 && a->out_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
   if (a->dtype == KDA_DTYPE_F32 && a->out_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
@@ -87,7 +89,7 @@ KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* a, cudaStream_t stream) {
   if (rc != KDA_OK) return rc;
   int path = a->path;
   if (path == KDA_PATH_AUTO) path = kda_select_path(a->dtype, a->dk, a->dv);
-  if (path == KDA_PATH_TC && !kda::tc_supported(a->dtype, a->dk, a->dv))
+  if (path == KDA_PATH_TC && (!kda::tc_supported(a->dtype, a->dk, a->dv) || a->gate != KDA_GATE_SIGMOID))
     return KDA_ERR_UNSUPPORTED_SHAPE;
   if (path == KDA_PATH_MMA && !kda::mma_supported(a->dtype, a->dk, a->dv))
     return KDA_ERR_UNSUPPORTED_SHAPE;
@@ -112,6 +114,7 @@ KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* a, cudaStream_t stream) {
   p.dv = a->dv;
   p.dtype = a->dtype;
   p.out_dtype = a->out_dtype;
+  p.gate = a->gate;
   if (empty && !a->cu_seqlens) {
     // no tokens: the final state is the initial state
     if (a->final_state) {
@@ -134,7 +137,7 @@ KDA_API int kda_chunk_fwd(const void* q, const void* k, const void* v, const voi
                           float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
                           int dk, int dv, cudaStream_t stream) {
   kda_fwd_args a{q, k, v, theta, beta, g_min, init_state, out, final_state, cu_seqlens,
-                 B, H, T, dk, dv, KDA_DTYPE_BF16, KDA_DTYPE_F32, KDA_PATH_AUTO};
+                 B, H, T, dk, dv, KDA_DTYPE_BF16, KDA_DTYPE_F32, KDA_PATH_AUTO, KDA_GATE_SIGMOID};
   return kda_chunk_fwd_ex(&a, stream);
 }
 
@@ -143,7 +146,7 @@ KDA_API int kda_chunk_fwd_f32(const float* q, const float* k, const float* v, co
                               float* final_state, const int32_t* cu_seqlens, int B, int H, int T,
                               int dk, int dv, cudaStream_t stream) {
   kda_fwd_args a{q, k, v, theta, beta, g_min, init_state, out, final_state, cu_seqlens,
-                 B, H, T, dk, dv, KDA_DTYPE_F32, KDA_DTYPE_F32, KDA_PATH_SIMT};
+                 B, H, T, dk, dv, KDA_DTYPE_F32, KDA_DTYPE_F32, KDA_PATH_SIMT, KDA_GATE_SIGMOID};
   return kda_chunk_fwd_ex(&a, stream);
 }
 
@@ -187,6 +190,7 @@ KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* a, int segments, void* w
   p.dv = a->dv;
   p.dtype = a->dtype;
   p.out_dtype = a->out_dtype;
+  p.gate = a->gate;
   return kda::launch_segmented(p, segments, workspace, workspace_bytes, stream);
 }
 

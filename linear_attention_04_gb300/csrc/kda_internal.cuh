@@ -30,6 +30,7 @@ struct FwdParams {
   int H, T, dk, dv;
   int dtype;                  // KDA_DTYPE_* of q, k, v, theta, beta
   int out_dtype;              // KDA_DTYPE_* of out
+  int gate;                   // KDA_GATE_*
 };
 
 // Validated parameters of one decode step (one token per sequence and head).

@@ -147,6 +147,7 @@ struct MmaArgs {
   const SegJob* jobs;  // per-CTA work units (segmented launches), or null
   const __nv_bfloat16* beta;
   float g_min;
+  int gate;
   const float* init_state;
   void* out;
   int out_bf16;
@@ -262,6 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (iw < nchunks) issued = 1;
     bool bad = false;
+    const bool log_decay = args.gate == KDA_GATE_LOG_DECAY;  // theta holds g itself
+    const f32x2 kL2 = f2(kLog2e, kLog2e);
     const f32x2 kC2 = f2(-kLog2e, -kLog2e);
     const f32x2 kC1 = f2(args.g_min * kLog2e, args.g_min * kLog2e);
     const f32x2 kOne = f2(1.0f, 1.0f);
@@ -289,12 +292,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) KTRACE(n, 6);
       if (nvalid < C) {
         // rows past the end of the sequence (the next sequence's tokens, or the
-        // zero fill past the tensor) become neutral: q = k = v = 0 and
-        // theta = -inf, i.e. g = 0 (no decay) and no contribution
+        // zero fill past the tensor) become neutral: q = k = v = 0 and g = 0 (no
+        // decay, no contribution): theta = -inf for the sigmoid gate, 0 when
+        // theta is the log-decay itself
         for (int e = lane; e < (C - nvalid) * 16; e += 32) {
           const int row = nvalid + (e >> 4), c16 = e & 15;
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-          const uint4 ninf = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+          const uint32_t tf = log_decay ? 0u : 0xff80ff80u;
+          const uint4 ninf = make_uint4(tf, tf, tf, tf);
           *(uint4*)(st + 0 * TILE + row * 256 + c16 * 16) = z;
           *(uint4*)(st + 1 * TILE + row * 256 + c16 * 16) = z;
           *(uint4*)(st + 2 * TILE + row * 256 + c16 * 16) = ninf;
@@ -318,8 +323,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const f32x2 x0 = mul2(bf2_to_f2(thw.x), kC2), x1 = mul2(bf2_to_f2(thw.y), kC2);
         const f32x2 d0 = add2(f2(ex2_approx(f2lo(x0)), ex2_approx(f2hi(x0))), kOne);
         const f32x2 d1 = add2(f2(ex2_approx(f2lo(x1)), ex2_approx(f2hi(x1))), kOne);
-        const f32x2 g0 = mul2(f2(rcp_approx(f2lo(d0)), rcp_approx(f2hi(d0))), kC1);
-        const f32x2 g1 = mul2(f2(rcp_approx(f2lo(d1)), rcp_approx(f2hi(d1))), kC1);
+        const f32x2 g0 = log_decay ? mul2(bf2_to_f2(thw.x), kL2)
+                                   : mul2(f2(rcp_approx(f2lo(d0)), rcp_approx(f2hi(d0))), kC1);
+        const f32x2 g1 = log_decay ? mul2(bf2_to_f2(thw.y), kL2)
+                                   : mul2(f2(rcp_approx(f2lo(d1)), rcp_approx(f2hi(d1))), kC1);
         G0 = add2(G0, g0);
         G1 = add2(G1, g1);
         const f32x2 e0 = f2(ex2_approx(f2lo(G0)), ex2_approx(f2hi(G0)));
@@ -705,6 +712,7 @@ int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStrea
   a.jobs = jobs;
   a.beta = (const __nv_bfloat16*)p.beta;
   a.g_min = p.g_min;
+  a.gate = p.gate;
   a.init_state = p.init_state;
   a.out = p.out;
   a.out_bf16 = p.out_dtype == KDA_DTYPE_BF16;

@@ -49,7 +49,7 @@ template <typename Tin, typename Tout, int DK, int DVS>
 __global__ void __launch_bounds__(kSimtThreads)
     kda_fwd_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                         const Tin* __restrict__ v, const Tin* __restrict__ theta,
-                        const Tin* __restrict__ beta, float g_min,
+                        const Tin* __restrict__ beta, float g_min, int gate,
                         const float* __restrict__ init_state, Tout* __restrict__ out,
                         float* __restrict__ final_state, const int32_t* __restrict__ cu_seqlens,
                         int N, int H, int T, int dv) {
@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kSimtThreads)
         if (r < n) {
           const int64_t row = (c0 + r) * H + h;
           float th = to_f32(theta[row * DK + col]);
-          float g = g_min * (1.0f / (1.0f + expf(-th)));
+          float g = gate == KDA_GATE_LOG_DECAY ? th : g_min * (1.0f / (1.0f + expf(-th)));
           G += g;
           kr[r] = to_f32(k[row * DK + col]);
           qr[r] = to_f32(q[row * DK + col]);
@@ -223,7 +223,7 @@ int launch_simt_t(const FwdParams& p, cudaStream_t stream) {
   dim3 grid((unsigned)(p.N * p.H), (unsigned)(p.dv / DVS));
   kern<<<grid, kSimtThreads, smem, stream>>>(
       (const Tin*)p.q, (const Tin*)p.k, (const Tin*)p.v, (const Tin*)p.theta, (const Tin*)p.beta,
-      p.g_min, p.init_state, (Tout*)p.out, p.final_state, p.cu_seqlens, p.N, p.H, p.T, p.dv);
+      p.g_min, p.gate, p.init_state, (Tout*)p.out, p.final_state, p.cu_seqlens, p.N, p.H, p.T, p.dv);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 

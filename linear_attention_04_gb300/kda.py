@@ -27,6 +27,7 @@ KDA_ERR_UNSUPPORTED_SHAPE = -7
 KDA_ERR_SCRATCH_TOO_SMALL = -8
 
 PATHS = {"auto": 0, "simt": 1, "tc": 2, "mma": 3}
+GATES = {"sigmoid": 0, "log_decay": 1}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
 _lock = threading.Lock()
@@ -46,7 +47,7 @@ class _Args(ctypes.Structure):
                 ("final_state", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
                 ("B", ctypes.c_int), ("H", ctypes.c_int), ("T", ctypes.c_int),
                 ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("dtype", ctypes.c_int),
-                ("out_dtype", ctypes.c_int), ("path", ctypes.c_int)]
+                ("out_dtype", ctypes.c_int), ("path", ctypes.c_int), ("gate", ctypes.c_int)]
 
 
 def library_path() -> str:
@@ -115,7 +116,8 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torc
                   init_state: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                   final_state: Optional[torch.Tensor] = None,
                   cu_seqlens: Optional[torch.Tensor] = None, *, want_final_state: bool = True,
-                  out_dtype: torch.dtype = torch.float32, path: str = "auto", stream=None):
+                  out_dtype: torch.dtype = torch.float32, path: str = "auto", gate: str = "sigmoid",
+                  stream=None):
     """KDA chunked forward through the C ABI (``kda_chunk_fwd_ex``).
 
     q, k, theta [B,T,H,dk]; v [B,T,H,dv]; beta [B,T,H], all bf16 or all fp32,
@@ -160,7 +162,7 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torc
         final_state = torch.empty(sshape, dtype=torch.float32, device=q.device)
     a = _Args(_ptr(q), _ptr(k), _ptr(v), _ptr(theta), _ptr(beta), float(g_min),
               _ptr(init_state), _ptr(out), _ptr(final_state), _ptr(cu_seqlens),
-              nseq, H, T, dk, dv, DTYPES[dtype], DTYPES[out_dtype], PATHS[path])
+              nseq, H, T, dk, dv, DTYPES[dtype], DTYPES[out_dtype], PATHS[path], GATES[gate])
     with torch.cuda.device(q.device):
         rc = lib.kda_chunk_fwd_ex(ctypes.byref(a), _stream_ptr(stream))
     if rc != KDA_OK:

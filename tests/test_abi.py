@@ -167,3 +167,16 @@ def test_noalloc_capacity_covers_the_long_workload():
     cap = 24 << 20
     assert lib.kda_segmented_workspace_size(1, 32, 262144, 128, 128, 5) <= cap
     assert lib.kda_segmented_workspace_size(1, 32, 262144, 128, 128, 6) > cap
+
+
+def test_gate_mode_host_checks():
+    lib = binding.load()
+    a = _args(gate=7)
+    assert lib.kda_chunk_fwd_ex(ctypes.byref(a), None) == binding.KDA_ERR_INVALID_ARG
+    # the log-decay gate ignores g_min, so g_min = 0 passes the argument check
+    # (and stops only at the device check on a machine without a GB300)
+    a = _args(gate=1, g_min=0.0)
+    assert lib.kda_chunk_fwd_ex(ctypes.byref(a), None) != binding.KDA_ERR_INVALID_ARG
+    # the tcgen05 path has only the bounded gate
+    a = _args(gate=1, path=2)
+    assert lib.kda_chunk_fwd_ex(ctypes.byref(a), None) == binding.KDA_ERR_UNSUPPORTED_SHAPE

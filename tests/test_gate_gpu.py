@@ -1,0 +1,70 @@
+"""The log-decay gate mode (theta holds g itself) against the oracle, and the
+unbounded -softplus control: with g = -softplus(theta) the in-chunk factor
+e^{-G} overflows once the logits are large, so the dense tile products stop
+being finite, while the bounded gate g_min * sigmoid(theta) on the very same
+logits never leaves e^{80} ("Architecture Deep Dive", sec. 3.2; "Kimi K3 Deep
+Dive", section "The Design")."""
+import numpy as np
+import pytest
+import torch
+
+from linear_attention_04_gb300 import kda_chunk_fwd, kda_device_status
+from linear_attention_04_gb300.workloads import Workload, make_inputs
+
+from parity import TOL, assert_close, f64
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(dtype, mu, seed, T=400, H=3):
+    w = Workload("gate", B=2, H=H, T=T, dk=128, dv=128, dtype=dtype)
+    inp = make_inputs(w, seed=seed)
+    logits = inp["theta"].float() + mu
+    g = -torch.nn.functional.softplus(logits)
+    return inp, logits.to(dtype), g.to(dtype)
+
+
+def _run(inp, theta, path, gate):
+    c = {k_: (x.cuda() if isinstance(x, torch.Tensor) else x) for k_, x in inp.items()}
+    o, S = kda_chunk_fwd(c["q"], c["k"], c["v"], theta.cuda(), c["beta"], -5.0, path=path,
+                         gate=gate)
+    torch.cuda.synchronize()
+    assert kda_device_status(clear=True) == 0
+    return o, S
+
+
+@pytest.mark.parametrize("dtype,path", [(torch.float32, "simt"), (torch.bfloat16, "simt"),
+                                        (torch.bfloat16, "mma")])
+def test_log_decay_gate_vs_oracle(dtype, path):
+    # logits ~ N(0.5, 1): |g| ~ 1 per token, inside the bf16 operand plan's
+    # precision envelope (slow-decay regimes are outside it for every gate)
+    inp, _, g = _case(dtype, mu=0.5, seed=31)
+    ro, rS = oracle.fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(g), f64(inp["beta"]),
+                        -5.0, None, theta_is_g=True)
+    o, S = _run(inp, g, path, "log_decay")
+    tol = TOL[dtype] if path == "mma" else TOL[torch.float32]
+    assert_close(f64(o), ro, tol, f"log-decay gate out ({path}, {dtype})")
+    assert_close(f64(S), rS, tol, f"log-decay gate state ({path}, {dtype})")
+
+
+def test_unbounded_softplus_control():
+    # logits ~ N(8, 1): every 16-token chunk reaches -G ~ 128 > 88.7 with the
+    # -softplus gate; the bounded gate on the same logits stays below 80
+    inp, logits, g = _case(torch.bfloat16, mu=8.0, seed=32)
+    G = -g.double().reshape(2, -1, 16, 3, 128).sum(dim=2)          # -G_16 per chunk
+    assert float(G.max()) > 88.72
+    gs = -5.0 * torch.sigmoid(logits.double())
+    assert float((-gs.reshape(2, -1, 16, 3, 128).sum(dim=2)).max()) <= 80.0
+    # the fp64 oracle is finite either way
+    ro, _ = oracle.fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(g), f64(inp["beta"]),
+                       -5.0, None, theta_is_g=True)
+    assert np.all(np.isfinite(ro))
+    # the dense tile path with the unbounded gate: not finite
+    o, _ = _run(inp, g, "mma", "log_decay")
+    assert not bool(torch.isfinite(o).all())
+    # the same logits through the bounded gate: finite and within the bar
+    rb, rSb = oracle.fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(logits),
+                         f64(inp["beta"]), -5.0, None)
+    ob, Sb = _run(inp, logits, "mma", "sigmoid")
+    assert_close(f64(ob), rb, TOL[torch.bfloat16], "bounded gate, same logits")
