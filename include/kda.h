@@ -179,6 +179,48 @@ KDA_API size_t kda_segmented_workspace_size(int B, int H, int T, int dk, int dv,
 KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* args, int segments, void* workspace,
                                     size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * kda_chunk_bwd -- gradients of kda_chunk_fwd's outputs and final state with
+ * respect to q, k, v, theta, beta and the initial state (the reverse pass of
+ * the recurrence of "Kimi K3 Deep Dive", section "Core Innovation 1"), in fp32
+ * on CUDA cores.  A correctness-first path: token-level reverse recursion,
+ * with the states before each token recomputed from block checkpoints in the
+ * caller's workspace.
+ * Requires dk = dv = 128 and a fixed-length batch.  Layouts as kda_chunk_fwd:
+ * q, k, theta, dq, dk, dtheta [B,T,H,dk]; v, d_out, dv [B,T,H,dv]; beta,
+ * dbeta [B,T,H]; init_state, d_final, d_init [B,H,dk,dv] fp32 (each of the
+ * three may be NULL: a zero initial state, no final-state gradient, not
+ * written).  `dtype` (KDA_DTYPE_*) is the type of q, k, v, theta, beta; every
+ * gradient and d_out/d_final are fp32.  `gate` as kda_fwd_args.gate.
+ * `workspace`: device memory of kda_chunk_bwd_workspace_size(B, H, T, dk, dv)
+ * bytes, 16-byte aligned, caller-owned, scratch until the stream has passed
+ * the call.  The library allocates nothing.  Returns KDA_OK or KDA_ERR_*.
+ */
+typedef struct kda_bwd_args {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* theta;
+  const void* beta;
+  float g_min;
+  const float* init_state;
+  const float* d_out;
+  const float* d_final;
+  float* dq;
+  float* dk;
+  float* dv;
+  float* dtheta;
+  float* dbeta;
+  float* d_init;
+  int B, H, T, dk_dim, dv_dim;
+  int dtype;
+  int gate;
+} kda_bwd_args;
+
+KDA_API size_t kda_chunk_bwd_workspace_size(int B, int H, int T, int dk, int dv);
+KDA_API int kda_chunk_bwd(const kda_bwd_args* args, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
 /* Bytes of the scratch area built into the library for
  * kda_chunk_fwd_segmented_noalloc (24 MiB per device). */
 #define KDA_NOALLOC_SCRATCH_BYTES (24u << 20)

@@ -209,6 +209,69 @@ KDA_API int kda_chunk_fwd_segmented_noalloc(const kda_fwd_args* a, int segments,
   return kda_chunk_fwd_segmented(a, segments, scratch, kda::kNoallocScratchBytes, stream);
 }
 
+KDA_API size_t kda_chunk_bwd_workspace_size(int B, int H, int T, int dk, int dv) {
+  if (B <= 0 || H <= 0 || T < 0 || dk != 128 || dv != 128) return 0;
+  return kda::bwd_workspace_size(B, H, T);
+}
+
+KDA_API int kda_chunk_bwd(const kda_bwd_args* a, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
+  if (!a) return KDA_ERR_INVALID_ARG;
+  if (a->B <= 0 || a->H <= 0 || a->T < 0) return KDA_ERR_INVALID_ARG;
+  if (a->dtype != KDA_DTYPE_BF16 && a->dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+  if (a->gate != KDA_GATE_SIGMOID && a->gate != KDA_GATE_LOG_DECAY) return KDA_ERR_INVALID_ARG;
+  if (a->gate == KDA_GATE_SIGMOID && (!(a->g_min < 0.0f) || a->g_min != a->g_min))
+    return KDA_ERR_INVALID_ARG;
+  if (a->dk_dim != 128 || a->dv_dim != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)a->B * a->H > (int64_t)INT32_MAX || (int64_t)a->B * a->T > ((int64_t)1 << 40))
+    return KDA_ERR_INVALID_ARG;
+  if (a->T > 0 && (!a->q || !a->k || !a->v || !a->theta || !a->beta || !a->d_out || !a->dq ||
+                   !a->dk || !a->dv || !a->dtheta || !a->dbeta))
+    return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {a->q, a->k, a->v, a->theta, a->beta, a->init_state, a->d_out, a->d_final,
+                        a->dq, a->dk, a->dv, a->dtheta, a->dbeta, a->d_init, workspace};
+  for (const void* p : ptrs)
+    if (p && !kda::aligned16(p)) return KDA_ERR_MISALIGNED;
+  const size_t need = kda::bwd_workspace_size(a->B, a->H, a->T);
+  if (a->T > 0 && (!workspace || workspace_bytes < need)) return KDA_ERR_INVALID_ARG;
+  const int rc = kda::check_device();
+  if (rc != KDA_OK) return rc;
+  if (a->T == 0) {
+    // no tokens: the initial state's gradient is the final state's
+    if (a->d_init) {
+      const size_t bytes = (size_t)a->B * a->H * 128 * 128 * sizeof(float);
+      const cudaError_t e = a->d_final ? cudaMemcpyAsync(a->d_init, a->d_final, bytes,
+                                                         cudaMemcpyDeviceToDevice, stream)
+                                       : cudaMemsetAsync(a->d_init, 0, bytes, stream);
+      if (e != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+  }
+  kda::BwdParams p;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.theta = a->theta;
+  p.beta = a->beta;
+  p.g_min = a->g_min;
+  p.gate = a->gate;
+  p.init_state = a->init_state;
+  p.d_out = a->d_out;
+  p.d_final = a->d_final;
+  p.dq = a->dq;
+  p.dk = a->dk;
+  p.dv = a->dv;
+  p.dtheta = a->dtheta;
+  p.dbeta = a->dbeta;
+  p.d_init = a->d_init;
+  p.workspace = workspace;
+  p.B = a->B;
+  p.H = a->H;
+  p.T = a->T;
+  p.dtype = a->dtype;
+  return kda::launch_bwd(p, stream);
+}
+
 KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const void* theta,
                             const void* beta, float g_min, float* state, float* out, int N, int H,
                             int dk, int dv, int dtype, cudaStream_t stream) {

@@ -49,6 +49,31 @@ struct DecodeParams {
 
 int launch_decode(const DecodeParams& p, cudaStream_t stream);
 
+// Validated parameters of the backward pass (fixed-length batches, dk = dv = 128).
+struct BwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* theta;
+  const void* beta;
+  float g_min;
+  int gate;
+  const float* init_state;  // [B, H, dk, dv] or null
+  const float* d_out;       // [B, T, H, dv]
+  const float* d_final;     // [B, H, dk, dv] or null
+  float* dq;                // [B, T, H, dk]
+  float* dk;
+  float* dv;                // [B, T, H, dv]
+  float* dtheta;            // [B, T, H, dk]
+  float* dbeta;             // [B, T, H]
+  float* d_init;            // [B, H, dk, dv] or null
+  void* workspace;
+  int B, H, T;
+  int dtype;
+};
+size_t bwd_workspace_size(int B, int H, int T);
+int launch_bwd(const BwdParams& p, cudaStream_t stream);
+
 // Device status word of the current device (bounded waits write it).
 int* status_word_device_ptr();
 

@@ -40,6 +40,14 @@ class KdaError(RuntimeError):
         super().__init__(f"{where}: {strerror(code)} (code {code})")
 
 
+class _BwdArgs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "theta", "beta")] + \
+        [("g_min", ctypes.c_float)] + \
+        [(n, ctypes.c_void_p) for n in ("init_state", "d_out", "d_final", "dq", "dk", "dv",
+                                        "dtheta", "dbeta", "d_init")] + \
+        [(n, ctypes.c_int) for n in ("B", "H", "T", "dk_dim", "dv_dim", "dtype", "gate")]
+
+
 class _Args(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("theta", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("g_min", ctypes.c_float),
@@ -78,6 +86,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                                     vp]
             lib.kda_chunk_fwd_segmented_noalloc.restype = i
             lib.kda_chunk_fwd_segmented_noalloc.argtypes = [ctypes.POINTER(_Args), i, vp]
+            lib.kda_chunk_bwd_workspace_size.restype = ctypes.c_size_t
+            lib.kda_chunk_bwd_workspace_size.argtypes = [i, i, i, i, i]
+            lib.kda_chunk_bwd.restype = i
+            lib.kda_chunk_bwd.argtypes = [ctypes.POINTER(_BwdArgs), vp, ctypes.c_size_t, vp]
             lib.kda_decode_step.restype = i
             lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp]
             lib.kda_chunk_fwd_ex.restype = i
@@ -236,6 +248,46 @@ def kda_chunk_fwd_segmented_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.T
     if rc != KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd_segmented_noalloc")
     return out, final_state
+
+
+def kda_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torch.Tensor,
+                  beta: torch.Tensor, d_out: torch.Tensor, g_min: float = -5.0,
+                  init_state: Optional[torch.Tensor] = None,
+                  d_final: Optional[torch.Tensor] = None, *, gate: str = "sigmoid",
+                  workspace: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Backward pass through the C ABI (``kda_chunk_bwd``): gradients of
+    sum(out * d_out) + sum(final_state * d_final) w.r.t. q, k, v, theta, beta
+    and init_state, as fp32 tensors in a dict (dq, dk, dv, dtheta, dbeta,
+    d_init).  Fixed-length batch, dk = dv = 128."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    for name, t, shape in (("k", k, (B, T, H, dk)), ("theta", theta, (B, T, H, dk)),
+                           ("v", v, (B, T, H, dv)), ("beta", beta, (B, T, H))):
+        if t.dtype != q.dtype or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name}: expected contiguous {q.dtype} {shape}")
+    if d_out.dtype != torch.float32 or tuple(d_out.shape) != (B, T, H, dv) or \
+            not d_out.is_contiguous():
+        raise ValueError(f"d_out: expected contiguous fp32 {(B, T, H, dv)}")
+    g = {"dq": torch.empty((B, T, H, dk), device=dev), "dk": torch.empty((B, T, H, dk), device=dev),
+         "dv": torch.empty((B, T, H, dv), device=dev),
+         "dtheta": torch.empty((B, T, H, dk), device=dev),
+         "dbeta": torch.empty((B, T, H), device=dev),
+         "d_init": torch.empty((B, H, dk, dv), device=dev)}
+    need = int(lib.kda_chunk_bwd_workspace_size(B, H, T, dk, dv))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    a = _BwdArgs(_ptr(q), _ptr(k), _ptr(v), _ptr(theta), _ptr(beta), float(g_min),
+                 _ptr(init_state), _ptr(d_out), _ptr(d_final), _ptr(g["dq"]), _ptr(g["dk"]),
+                 _ptr(g["dv"]), _ptr(g["dtheta"]), _ptr(g["dbeta"]), _ptr(g["d_init"]),
+                 B, H, T, dk, dv, DTYPES[q.dtype], GATES[gate])
+    with torch.cuda.device(dev):
+        rc = lib.kda_chunk_bwd(ctypes.byref(a), _ptr(workspace), workspace.numel(),
+                               _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_bwd")
+    return g
 
 
 def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torch.Tensor,

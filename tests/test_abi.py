@@ -180,3 +180,37 @@ def test_gate_mode_host_checks():
     # the tcgen05 path has only the bounded gate
     a = _args(gate=1, path=2)
     assert lib.kda_chunk_fwd_ex(ctypes.byref(a), None) == binding.KDA_ERR_UNSUPPORTED_SHAPE
+
+
+def _bwd_args(**over):
+    a = dict(q=0x1000, k=0x2000, v=0x3000, theta=0x4000, beta=0x5000, g_min=-5.0,
+             init_state=None, d_out=0x6000, d_final=None, dq=0x7000, dk=0x8000, dv=0x9000,
+             dtheta=0xa000, dbeta=0xb000, d_init=None, B=1, H=2, T=64, dk_dim=128, dv_dim=128,
+             dtype=0, gate=0)
+    a.update(over)
+    return binding._BwdArgs(**a)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dq=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(d_out=None), binding.KDA_ERR_INVALID_ARG),
+    (dict(B=0), binding.KDA_ERR_INVALID_ARG),
+    (dict(g_min=1.0), binding.KDA_ERR_INVALID_ARG),
+    (dict(gate=5), binding.KDA_ERR_INVALID_ARG),
+    (dict(dk_dim=64), binding.KDA_ERR_UNSUPPORTED_SHAPE),
+    (dict(dtheta=0xa004), binding.KDA_ERR_MISALIGNED),
+])
+def test_bwd_host_side_rejection(over, code):
+    lib = binding.load()
+    a = _bwd_args(**over)
+    assert lib.kda_chunk_bwd(ctypes.byref(a), 0x100000, 1 << 40, None) == code
+
+
+def test_bwd_workspace_rules():
+    lib = binding.load()
+    n = lib.kda_chunk_bwd_workspace_size(1, 2, 64, 128, 128)
+    assert n == 2 * (1 + 64) * 128 * 128 * 4
+    assert lib.kda_chunk_bwd_workspace_size(1, 2, 64, 64, 128) == 0
+    a = _bwd_args()
+    assert lib.kda_chunk_bwd(ctypes.byref(a), 0x100000, n - 1, None) == binding.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_bwd(ctypes.byref(a), None, n, None) == binding.KDA_ERR_INVALID_ARG
