@@ -541,6 +541,69 @@ def run_decode(args, rank, world, local):
             "clocks": clocks.summary(t_wall0, t_wall1)}
 
 
+# ----------------------------------------------------------------------------- backward
+
+def bwd_bytes(w, inp, e=2) -> int:
+    """HBM bytes of one backward pass (token-heads x per-token-head bytes): the
+    bf16 inputs, the fp32 d_out, the fp32 gradients dq, dk, dtheta, dv, dbeta."""
+    n = n_tokens(inp) * w.H
+    return n * (e * (3 * w.dk + w.dv) + e + 4 * w.dv + 4 * (3 * w.dk + w.dv) + 4)
+
+
+def run_bwd(args, rank, world, local):
+    from linear_attention_04_gb300 import kda_chunk_bwd, kda_device_status
+    from linear_attention_04_gb300 import kda as binding
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = selected_workload(args)
+    if w.varlen:
+        raise SystemExit("the backward takes fixed-length batches")
+    inp = make_inputs(w, seed=rank_seed(args.seed, rank), device=dev)
+    g = torch.Generator(device="cpu").manual_seed(args.seed + 3)
+    d_out = torch.randn(w.B, w.T, w.H, w.dv, generator=g).to(dev)
+    ws = torch.empty(binding.load().kda_chunk_bwd_workspace_size(w.B, w.H, w.T, w.dk, w.dv),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda_chunk_bwd(inp["q"], inp["k"], inp["v"], inp["theta"], inp["beta"], d_out, w.g_min,
+                      inp["init_state"], None, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if kda_device_status(clear=True) != 0:
+        raise RuntimeError("device status after warm-up")
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    total_ms = max_over_ranks(start.elapsed_time(end), world)
+    step_s = total_ms / args.steps / 1e3
+    peaks, peak_src = measured_peaks()
+    nbytes = bwd_bytes(w, inp)
+    achieved = nbytes / step_s / 1e9
+    tokens = n_tokens(inp)
+    return {"metric": "KDA backward tokens/s (all gradients of the forward pass)",
+            "value": tokens * world / step_s, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "op": "bwd",
+            "config": {"workload": f"{w.name}: B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv}, "
+                                   "fp32 arithmetic on CUDA cores"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 5),
+                         "traffic": None, "peak_source": f"hbm_gbs of {peak_src}",
+                         "kernel": "kda_bwd_kernel", "algorithmic_bytes_per_launch": nbytes},
+            "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -558,8 +621,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--segments", type=int, default=1,
                     help="fwd: cut each sequence into this many segments (segment-parallel path)")
-    ap.add_argument("--op", choices=["fwd", "decode"], default="fwd",
-                    help="fwd: the chunked forward (the headline); decode: one recurrent step")
+    ap.add_argument("--op", choices=["fwd", "decode", "bwd"], default="fwd",
+                    help="fwd: the chunked forward (the headline); decode: one recurrent step; "
+                         "bwd: the backward pass")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("note: at least 3 warm-up steps are required; using 3", file=sys.stderr)
@@ -577,7 +641,8 @@ def main(argv=None):
                 return 0
             line = run_reference(args, rank, world)
         else:
-            line = (run_decode if args.op == "decode" else run_ours)(args, rank, world, local)
+            line = {"decode": run_decode, "bwd": run_bwd}.get(args.op, run_ours)(args, rank, world,
+                                                                            local)
         if rank == 0:
             print(json.dumps(line), flush=True)
     finally:

@@ -29,7 +29,7 @@
 //   warps 4..7  intra warps: warp 4+i runs chunks i, i+4, i+8, ...; each
 //               loads its chunk with TMA (q, k, theta, v into a private stage,
 //               refilled with its next chunk as soon as the stage is read),
-//               computes the gate g = g_min * sigmoid(theta), the cumulative
+//               computes the gate (g = g_min * sigmoid(theta)), the cumulative
 //               sums and the decayed operands in fp32, the chunk products A, P
 //               and W = Tb Kt with mma.sync, the triangular inverse by forward
 //               substitution, and fills a chunk slot for the state warps.
@@ -42,6 +42,13 @@
 //
 // The diagonal of Qt Kh^T is q_t . k_t exactly (the decay factors cancel), so
 // it is taken in fp32 from the bf16 inputs and applied to U in fp32.
+//
+// A CTA runs either one whole (sequence, head) chain or, in a segmented
+// launch, one job of a table (token range, head, initial and final state, and
+// options: v taken as zero, no outputs, identity initial state), which is how
+// the segment-parallel forward obtains each segment's linear part and local
+// state.  The gate is g_min * sigmoid(theta), or theta itself as a given
+// log-decay.
 //
 // Every wait is bounded: a wait that runs out sets the CTA's abort flag and the
 // device status word (KDA_ERR_DEVICE_TIMEOUT); every role then leaves its loop

@@ -15,6 +15,8 @@ Parity status of each function (what pins it is listed in the tests):
              linearity, column independence, varlen independence)
   gate       pinned (closed form values of the sigmoid, range [g_min, 0])
   chunked    pinned against ``fwd`` (chunk-size invariance)
+  backward   (oracle/backward.py) pinned: its forward equals ``fwd``; its
+             gradients equal central finite differences of ``fwd``
 """
 from __future__ import annotations
 
