@@ -37,9 +37,10 @@ def _run(inp, theta, path, gate):
 @pytest.mark.parametrize("dtype,path", [(torch.float32, "simt"), (torch.bfloat16, "simt"),
                                         (torch.bfloat16, "mma")])
 def test_log_decay_gate_vs_oracle(dtype, path):
-    # logits ~ N(0.5, 1): |g| ~ 1 per token, inside the bf16 operand plan's
-    # precision envelope (slow-decay regimes are outside it for every gate)
-    inp, _, g = _case(dtype, mu=0.5, seed=31)
+    # logits ~ N(2, 1): |g| ~ 2.2 per token, the decay rate of the named
+    # workloads (the bf16 operand plan's error grows past the 2e-2 bar once the
+    # in-chunk decay is much slower, for either gate)
+    inp, _, g = _case(dtype, mu=2.0, seed=31)
     ro, rS = oracle.fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(g), f64(inp["beta"]),
                         -5.0, None, theta_is_g=True)
     o, S = _run(inp, g, path, "log_decay")
