@@ -221,6 +221,22 @@ KDA_API size_t kda_chunk_bwd_workspace_size(int B, int H, int T, int dk, int dv)
 KDA_API int kda_chunk_bwd(const kda_bwd_args* args, void* workspace, size_t workspace_bytes,
                           cudaStream_t stream);
 
+/*
+ * kda_selftest_withheld_handoff -- test hook for the failure path (no
+ * counterpart on the pages).  Runs the register-resident kernel on the first
+ * (sequence, head) chain of `args` (bf16, dk = dv = 128, fixed length,
+ * T >= 16) with the producer side withholding the hand-off of the first
+ * chunk, and every bounded wait limited to `wait_limit_ns` (> 0).  The
+ * consumer's wait runs out, the kernel stops all its roles, and the device
+ * status word reads KDA_ERR_DEVICE_TIMEOUT after the stream is synchronised
+ * (kda_device_status); the context stays usable.  Nothing is faulted or hung.
+ * `workspace`: 256 bytes of caller device memory (the job descriptor).
+ * Outputs are left incomplete.  Returns KDA_OK if the launch was made.
+ */
+KDA_API int kda_selftest_withheld_handoff(const kda_fwd_args* args, long long wait_limit_ns,
+                                          void* workspace, size_t workspace_bytes,
+                                          cudaStream_t stream);
+
 /* Bytes of the scratch area built into the library for
  * kda_chunk_fwd_segmented_noalloc (24 MiB per device). */
 #define KDA_NOALLOC_SCRATCH_BYTES (24u << 20)

@@ -272,6 +272,50 @@ KDA_API int kda_chunk_bwd(const kda_bwd_args* a, void* workspace, size_t workspa
   return kda::launch_bwd(p, stream);
 }
 
+KDA_API int kda_selftest_withheld_handoff(const kda_fwd_args* a, long long wait_limit_ns,
+                                          void* workspace, size_t workspace_bytes,
+                                          cudaStream_t stream) {
+  int rc = kda::validate(a);
+  if (rc != KDA_OK) return rc;
+  if (a->dtype != KDA_DTYPE_BF16 || a->dk != 128 || a->dv != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+  if (a->cu_seqlens || a->T < 16 || wait_limit_ns <= 0) return KDA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < sizeof(kda::SegJob)) return KDA_ERR_INVALID_ARG;
+  if (!kda::aligned16(workspace)) return KDA_ERR_MISALIGNED;
+  rc = kda::check_device();
+  if (rc != KDA_OK) return rc;
+  kda::SegJob job;
+  job.t0 = 0;
+  job.t1 = a->T;
+  job.head = 0;
+  job.flags = kda::kJobTestWithholdFirst;
+  job.init = a->init_state;
+  job.final_state = a->final_state;
+  if (cudaMemcpyAsync(workspace, &job, sizeof(job), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  kda::FwdParams p;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.theta = a->theta;
+  p.beta = a->beta;
+  p.g_min = a->g_min;
+  p.init_state = a->init_state;
+  p.out = a->out;
+  p.final_state = a->final_state;
+  p.cu_seqlens = nullptr;
+  p.N = 1;
+  p.H = a->H;
+  p.T = (int)((int64_t)a->B * a->T);
+  p.dk = a->dk;
+  p.dv = a->dv;
+  p.dtype = a->dtype;
+  p.out_dtype = a->out_dtype;
+  p.gate = a->gate;
+  // the job table lives in device memory the copy above fills, in stream order
+  rc = kda::launch_mma_jobs(p, (const kda::SegJob*)workspace, 1, stream, (uint64_t)wait_limit_ns);
+  return rc;
+}
+
 KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const void* theta,
                             const void* beta, float g_min, float* state, float* out, int N, int H,
                             int dk, int dv, int dtype, cudaStream_t stream) {

@@ -87,6 +87,7 @@ int launch_mma(const FwdParams& p, cudaStream_t stream);
 constexpr int kJobZeroV = 1;          // V is taken as zero (the state's linear part)
 constexpr int kJobNoOut = 2;          // no output stores
 constexpr int kJobIdentityInit = 4;   // initial state = identity (dk = dv), init ignored
+constexpr int kJobTestWithholdFirst = 8;  // test only: the first chunk's hand-off is never made
 struct SegJob {
   int64_t t0, t1;          // token rows [t0, t1) of the packed [tokens, H, .] tensors
   int head;
@@ -94,8 +95,10 @@ struct SegJob {
   const float* init;       // [dk][dv] initial state, or null (zero / identity)
   float* final_state;      // [dk][dv] end state, or null
 };
-// Launches one CTA per job over the packed token axis (p.T = total tokens).
-int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStream_t stream);
+// Launches one CTA per job over the packed token axis (p.T = total tokens);
+// wait_ns = 0 keeps the default limit of the bounded waits.
+int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStream_t stream,
+                    uint64_t wait_ns = 0);
 
 // Segment-parallel forward (fixed-length batches, bf16, dk = dv = 128): the
 // scratch it needs and the launch sequence over a caller-provided workspace.

@@ -82,7 +82,7 @@ constexpr int kThreads = 32 * (kStateWarps + kIntraWarps);
 // checks it against the compiled register count before the first launch.
 constexpr int kStateRegs = 0, kIntraRegs = 0;
 constexpr int NSLOT = 6;  // chunk slots between the intra and the state warps
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
+constexpr uint64_t kWaitNs = 2000000000ull;  // default limit of every wait: 2 s
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- shared memory
@@ -152,6 +152,7 @@ __device__ __forceinline__ void set_regs() {
 
 struct MmaArgs {
   const SegJob* jobs;  // per-CTA work units (segmented launches), or null
+  uint64_t wait_ns;    // limit of every bounded wait
   const __nv_bfloat16* beta;
   float g_min;
   int gate;
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // beta of the chunk (lane t holds beta_t), issued before the waits
       float beta_l = 0.0f;
       if (lane < nvalid) beta_l = __bfloat162float(args.beta[(ch.t0 + (int64_t)n * C + lane) * H + h]);
-      if (!__all_sync(0xffffffffu, mbar_wait(full, consumed & 1, abort, kWaitNs))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(full, consumed & 1, abort, args.wait_ns))) {
         bad = true;
         break;
       }
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) KTRACE(n, 5);
       if (n >= NSLOT &&
           !__all_sync(0xffffffffu,
-                      mbar_wait(&bars[B_FREE + slot], ((n / NSLOT) - 1) & 1, abort, kWaitNs))) {
+                      mbar_wait(&bars[B_FREE + slot], ((n / NSLOT) - 1) & 1, abort, args.wait_ns))) {
         bad = true;
         break;
       }
@@ -485,7 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      if (lane == 0) {
+      // (a test job can withhold its first hand-off: the state warps' bounded
+      // wait then runs out and reports KDA_ERR_DEVICE_TIMEOUT)
+      if (lane == 0 && !(n == 0 && (*sflags & kJobTestWithholdFirst))) {
         mbar_arrive(&bars[B_READY + slot]);
         KTRACE(n, 10);
       }
@@ -493,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (bad) fail(abort, args.status);
     // a refill issued for a chunk this warp never waited for is drained
     // before the CTA releases its shared memory
-    if (lane == 0 && issued > consumed) mbar_wait_drain(full, consumed & 1, kWaitNs);
+    if (lane == 0 && issued > consumed) mbar_wait_drain(full, consumed & 1, args.wait_ns);
   } else {
     // ================================================================ state warps
     if constexpr (kStateRegs > 0) set_regs<kStateRegs>();
@@ -518,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned char* sl = sm + SM_SLOTS + slot * SLOT_BYTES;
       const uint32_t sls = sbase + SM_SLOTS + slot * SLOT_BYTES;
       if (!__all_sync(0xffffffffu,
-                      mbar_wait(&bars[B_READY + slot], (n / NSLOT) & 1, abort, kWaitNs))) {
+                      mbar_wait(&bars[B_READY + slot], (n / NSLOT) & 1, abort, args.wait_ns))) {
         bad = true;
         break;
       }
@@ -684,7 +687,8 @@ bool mma_supported(int dtype, int dk, int dv) {
   return dtype == KDA_DTYPE_BF16 && dk == D && dv == D;
 }
 
-int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStream_t stream) {
+int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStream_t stream,
+                    uint64_t wait_ns) {
   if (!mma_supported(p.dtype, p.dk, p.dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
   const int64_t tokens = p.cu_seqlens ? (int64_t)p.T : (int64_t)p.N * p.T;
   if (tokens <= 0) {
@@ -729,6 +733,7 @@ int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStrea
   a.H = p.H;
   a.T = p.T;
   a.status = status_word_device_ptr();
+  a.wait_ns = wait_ns ? wait_ns : kWaitNs;
   if (!a.status) return KDA_ERR_CUDA;
   const unsigned grid = jobs ? (unsigned)njobs : (unsigned)(p.N * p.H);
   if (grid == 0) return KDA_OK;

@@ -90,6 +90,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.kda_chunk_bwd_workspace_size.argtypes = [i, i, i, i, i]
             lib.kda_chunk_bwd.restype = i
             lib.kda_chunk_bwd.argtypes = [ctypes.POINTER(_BwdArgs), vp, ctypes.c_size_t, vp]
+            lib.kda_selftest_withheld_handoff.restype = i
+            lib.kda_selftest_withheld_handoff.argtypes = [ctypes.POINTER(_Args), ctypes.c_longlong,
+                                                          vp, ctypes.c_size_t, vp]
             lib.kda_decode_step.restype = i
             lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp]
             lib.kda_chunk_fwd_ex.restype = i

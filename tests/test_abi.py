@@ -214,3 +214,16 @@ def test_bwd_workspace_rules():
     a = _bwd_args()
     assert lib.kda_chunk_bwd(ctypes.byref(a), 0x100000, n - 1, None) == binding.KDA_ERR_INVALID_ARG
     assert lib.kda_chunk_bwd(ctypes.byref(a), None, n, None) == binding.KDA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("over,limit,ws,code", [
+    (dict(), 0, 0x10000, binding.KDA_ERR_INVALID_ARG),
+    (dict(T=8), 1000000, 0x10000, binding.KDA_ERR_INVALID_ARG),
+    (dict(), 1000000, None, binding.KDA_ERR_INVALID_ARG),
+    (dict(dtype=1), 1000000, 0x10000, binding.KDA_ERR_UNSUPPORTED_SHAPE),
+    (dict(), 1000000, 0x10008, binding.KDA_ERR_MISALIGNED),
+])
+def test_selftest_hook_host_side_rejection(over, limit, ws, code):
+    lib = binding.load()
+    a = _args(**over)
+    assert lib.kda_selftest_withheld_handoff(ctypes.byref(a), limit, ws, 256, None) == code
