@@ -1,22 +1,39 @@
-// kda_bwd.cu -- backward pass of the KDA recurrence (gradients of the forward
-// pass w.r.t. q, k, v, theta, beta and the initial state), fp32 on CUDA cores.
+// kda_bwd.cu -- backward pass of KDA in chunked (WY) form, fp32 on CUDA cores.
 //
-// Forward ("Kimi K3 Deep Dive", section "Core Innovation 1"; gate of
-// "Architecture Deep Dive", sec. 3.2), per (sequence, head), token t:
-//   X = Diag(e^{g}) S_{t-1},  u = beta (v - X^T k),  S_t = X + k u^T,  o = S_t^T q.
-// Reverse pass with L = dL/dS_t (the gradient flowing back from later tokens
-// plus q do^T from this token's output):
-//   dq = S_t do,  kL = L^T k,  dv = beta kL,  dbeta = kL . (v - X^T k),
-//   dk = L u - beta X kL,  dX = L - beta k kL^T,  dg_i = sum_j dX_ij X_ij,
-//   dtheta = dg * g_min sigmoid(theta) (1 - sigmoid(theta))  (or dg for a given
-//   log-decay),  L <- Diag(e^{g}) dX  (the gradient w.r.t. S_{t-1}).
+// Forward, per (sequence, head) and 16-token chunk ("Kimi K3 Deep Dive",
+// section "Core Innovation 1"; gate of "Architecture Deep Dive", sec. 3.2),
+// with the inclusive in-chunk cumulative log-decay G, Kt = K e^{G},
+// Qt = Q e^{G}, Kh = K e^{-G}, KhC = K e^{G_C - G}, ec = e^{G_C}:
+//   Ab = strict_lower(Kt Kh^T),  M = (I + Diag(b) Ab)^{-1},  Tb = M Diag(b)
+//   Pi = lower_incl_diag(Qt Kh^T)
+//   R = V - Kt S,  U = Tb R,  O = Qt S + Pi U,  S' = Diag(ec) S + KhC^T U
+// Reverse-mode differentiation of these steps, with dO the output gradient
+// and dS' the gradient w.r.t. the chunk's end state:
+//   dU = Pi^T dO + KhC dS'            dR = Tb^T dU        dV = dR
+//   dS = Diag(ec) dS' + Qt^T dO - Kt^T dR                (carried backwards)
+//   dTb = lower_incl_diag(dU R^T)     dPi = lower_incl_diag(dO U^T)
+//   dQt = dO S^T + dPi Kh             dKhC = U dS'^T      dec = rowsum(dS' * S)
+//   (the diagonal of dPi goes straight to dq_t += dPi_tt k_t, dk_t += dPi_tt q_t:
+//   Pi_tt = q_t . k_t has no decay factor, and its shares of dG cancel exactly)
+//   dA = -strict_lower(M^T (dTb Diag(b)) M^T)
+//   db_j = sum_i M_ij dTb_ij + sum_l dA_jl Ab_jl
+//   dKt = -dR S^T + Diag(b) dA Kh     dKh = dPi^T Qt + (Diag(b) dA)^T Kt
+//   dK = dKt e^{G} + dKh e^{-G} + dKhC e^{G_C - G},   dQ = dQt e^{G}
+//   dG = dKt Kt + dQt Qt - dKh Kh - dKhC KhC (elementwise),
+//   dG_C = colsum(dKhC KhC) + dec ec,   dg_t = sum_{s >= t} dG_s + dG_C,
+//   (summed as sum_{s >= t} (dG_s + dKhC_s KhC_s) + sum_{s < t} dKhC_s KhC_s + dec ec),
+//   dtheta = dg g_min sigmoid(theta) sigmoid(-theta)   (dg for a given log-decay).
 //
-// One CTA per chain, 256 threads in a 16 x 16 grid; thread (r, c) holds the
-// 8 x 8 tiles [8r, 8r+8) x [8c, 8c+8) of S and L in registers.  Row and column
-// sums go through shared memory (16 partials per row or column).  States
-// before each token come from a two-level recomputation over the caller's
-// workspace: the state every kBlock tokens (forward pass), then, per block in
-// reverse order, the kBlock states of the block.
+// Three launches over a caller workspace:
+//   1. kda_bwd_states_kernel  (one CTA per chain): the forward recurrence,
+//      writing the state at the start of every chunk;
+//   2. kda_bwd_reverse_kernel (one CTA per chain): the reverse recurrence of
+//      dS, writing dS' and dU of every chunk, and dV;
+//   3. kda_bwd_grads_kernel   (one CTA per chunk, all chunks in parallel):
+//      every other gradient from S, dS', dU and the chunk's inputs.
+// Launches 1 and 2 carry their 128 x 128 state in registers (an 8 x 8 tile
+// per thread) with a copy in shared memory for the products that contract
+// over it.  Every product is an fp32 FMA over shared-memory operands.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -27,277 +44,753 @@
 namespace kda {
 namespace {
 
-constexpr int D = 128;         // dk = dv
-constexpr int TT = 8;          // tile edge per thread
-constexpr int NT = D / TT;     // 16 tiles per edge
-constexpr int kThreads = NT * NT;
-constexpr int kBlock = 64;     // tokens per recomputation block
-constexpr size_t kState = (size_t)D * D;  // floats per state
+constexpr int C = kChunk;             // 16
+constexpr int D = 128;                // dk = dv
+constexpr int LD = D + 4;             // row stride (floats) of 16 x 128 tiles and of the state
+constexpr int LS = 20;                // row stride of 16 x 16 matrices
+constexpr int kThreads = 256;
+constexpr int TILE_F = C * LD;        // floats of a token tile
+constexpr int STATE_F = D * LD;       // floats of the padded state
+constexpr int SM16_F = C * LS;        // floats of a 16 x 16 matrix
+constexpr size_t kStateF = (size_t)D * D;  // floats of one state in the workspace
 
-struct BwdShared {
-  float q[D], k[D], e[D], dgate[D];  // token vectors (e = e^{g}, dgate = dg/dtheta)
-  float v[D], dout[D];
-  float colp[NT][D];   // column partial sums (one per tile row)
-  float rowp[NT][D];   // row partial sums (one per tile column)
-  float vec[3][D];     // reduced vectors: u, kL, kL * (v - X^T k)
-  float beta;
+struct BwdDev {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* theta;
+  const void* beta;
+  float g_min;
+  int log_decay;
+  const float* init_state;
+  const float* d_out;
+  const float* d_final;
+  float* dq;
+  float* dk;
+  float* dv;
+  float* dtheta;
+  float* dbeta;
+  float* d_init;
+  float* ws_S;   // [chain][chunk][128][128] state at each chunk start
+  float* ws_dS;  // [chain][chunk][128][128] gradient w.r.t. each chunk's end state
+  float* ws_dU;  // [chain][chunk][16][128]
+  int H, T, nch;
 };
 
-template <typename Tin>
-__device__ __forceinline__ void load_token(BwdShared& sh, const Tin* q, const Tin* k, const Tin* v,
-                                           const Tin* theta, const Tin* beta, const float* dout,
-                                           int64_t row, float g_min, int gate, int tid) {
-  if (tid < D) {
-    const float th = to_f32(theta[row * D + tid]);
-    float g, dg;
-    if (gate == KDA_GATE_LOG_DECAY) {
-      g = th;
-      dg = 1.0f;
+// acc[m][t] += sum_{k0 <= k < k1} A(m0 + m, k) B(k, col(t)), operands in shared
+// memory.  A: A[m * lda + k] (AMK) or A[k * lda + m].  B: BKN -> B[k * ldb +
+// col] with col(t) = n0 + (t / 4) * nstride + t % 4 (groups of four adjacent
+// columns); else B[col * ldb + k] with col(t) = n0 + t * nstride.  k runs in
+// steps of four (float4 loads along the contiguous dimension).
+template <int TM, int TN, bool AMK, bool BKN>
+__device__ __forceinline__ void gemm_acc(float (&acc)[TM][TN], const float* A, int lda, int m0,
+                                         const float* B, int ldb, int n0, int nstride, int k0,
+                                         int k1) {
+  static_assert(AMK || TM % 4 == 0, "k-major A needs TM % 4 == 0");
+  static_assert(!BKN || TN % 4 == 0, "k-major B needs TN % 4 == 0");
+  for (int k = k0; k < k1; k += 4) {
+    float a[TM][4], b[4][TN];
+    if constexpr (AMK) {
+#pragma unroll
+      for (int m = 0; m < TM; ++m) {
+        const float4 x = *(const float4*)(A + (m0 + m) * lda + k);
+        a[m][0] = x.x;
+        a[m][1] = x.y;
+        a[m][2] = x.z;
+        a[m][3] = x.w;
+      }
     } else {
-      const float s = 1.0f / (1.0f + expf(-th));
-      g = g_min * s;
-      dg = g_min * s * (1.0f - s);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int m4 = 0; m4 < TM; m4 += 4) {
+          const float4 x = *(const float4*)(A + (k + kk) * lda + m0 + m4);
+          a[m4][kk] = x.x;
+          a[m4 + 1][kk] = x.y;
+          a[m4 + 2][kk] = x.z;
+          a[m4 + 3][kk] = x.w;
+        }
     }
-    sh.e[tid] = expf(g);
-    sh.dgate[tid] = dg;
-    sh.q[tid] = to_f32(q[row * D + tid]);
-    sh.k[tid] = to_f32(k[row * D + tid]);
-  } else {
-    const int j = tid - D;
-    sh.v[j] = to_f32(v[row * D + j]);
-    sh.dout[j] = dout ? dout[row * D + j] : 0.0f;
+    if constexpr (BKN) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int g4 = 0; g4 < TN / 4; ++g4) {
+          const float4 x = *(const float4*)(B + (k + kk) * ldb + n0 + g4 * nstride);
+          b[kk][4 * g4] = x.x;
+          b[kk][4 * g4 + 1] = x.y;
+          b[kk][4 * g4 + 2] = x.z;
+          b[kk][4 * g4 + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+      for (int t = 0; t < TN; ++t) {
+        const float4 x = *(const float4*)(B + (n0 + t * nstride) * ldb + k);
+        b[0][t] = x.x;
+        b[1][t] = x.y;
+        b[2][t] = x.z;
+        b[3][t] = x.w;
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int m = 0; m < TM; ++m)
+#pragma unroll
+        for (int t = 0; t < TN; ++t) acc[m][t] = fmaf(a[m][kk], b[kk][t], acc[m][t]);
   }
-  if (tid == 0) sh.beta = to_f32(beta[row]);
 }
 
-// S <- X + k u^T with X = Diag(e) S, u = beta (v - X^T k); tile form.
-__device__ __forceinline__ void fwd_step(BwdShared& sh, float (&S)[TT][TT], int r, int c, int tid) {
+// Partial sums of a 16 x 128 product with K = 128 split four ways:
+// part[ks][m][n] = sum_{32 ks <= k < 32 ks + 32} A[m][k] B(k, n).  A is a
+// token tile (row-major, k contiguous).  B is the padded 128 x 128 state,
+// read as B[k][n] (BKN) or B[n][k].
+template <bool BKN>
+__device__ __forceinline__ void part16(const float* A, const float* B, float* part) {
+  const int tid = threadIdx.x, ng = tid & 31, mg = (tid >> 5) & 1, ks = tid >> 6;
+  float acc[8][4];
 #pragma unroll
-  for (int a = 0; a < TT; ++a)
+  for (int m = 0; m < 8; ++m)
 #pragma unroll
-    for (int b = 0; b < TT; ++b) S[a][b] *= sh.e[TT * r + a];
-  // column sums of k_i X_ij
+    for (int t = 0; t < 4; ++t) acc[m][t] = 0.0f;
+  if constexpr (BKN) {
+    gemm_acc<8, 4, true, true>(acc, A, LD, 8 * mg, B, LD, 4 * ng, 0, 32 * ks, 32 * ks + 32);
 #pragma unroll
-  for (int b = 0; b < TT; ++b) {
-    float p = 0.0f;
+    for (int m = 0; m < 8; ++m)
+      *(float4*)(part + (ks * C + 8 * mg + m) * LD + 4 * ng) =
+          make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+  } else {
+    gemm_acc<8, 4, true, false>(acc, A, LD, 8 * mg, B, LD, ng, 32, 32 * ks, 32 * ks + 32);
 #pragma unroll
-    for (int a = 0; a < TT; ++a) p = fmaf(sh.k[TT * r + a], S[a][b], p);
-    sh.colp[r][TT * c + b] = p;
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) part[(ks * C + 8 * mg + m) * LD + ng + 32 * t] = acc[m][t];
+  }
+}
+
+// Partial sums of a 32 x 128 product X B^T (K = 128 split two ways); X is 32
+// token rows (row-major), B the padded state read as B[n][k].
+__device__ __forceinline__ void part32_nk(const float* X, const float* B, float* part) {
+  const int tid = threadIdx.x, ng = tid & 31, mg = (tid >> 5) & 3, ks = tid >> 7;
+  float acc[8][4];
+#pragma unroll
+  for (int m = 0; m < 8; ++m)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) acc[m][t] = 0.0f;
+  gemm_acc<8, 4, true, false>(acc, X, LD, 8 * mg, B, LD, ng, 32, 64 * ks, 64 * ks + 64);
+#pragma unroll
+  for (int m = 0; m < 8; ++m)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) part[(ks * 2 * C + 8 * mg + m) * LD + ng + 32 * t] = acc[m][t];
+}
+
+// out[m][n] = base[m][n] + sign * sum_s part[s][m][n] over an M x 128 tile
+// (base may be null; out may alias base or part[0]).
+template <int M, int KS>
+__device__ __forceinline__ void reduce_parts(const float* part, float* out, const float* base,
+                                             float sign) {
+  for (int e = threadIdx.x; e < M * (D / 4); e += kThreads) {
+    const int m = e >> 5, n = (e & 31) * 4;
+    float4 s = *(const float4*)(part + m * LD + n);
+#pragma unroll
+    for (int ks = 1; ks < KS; ++ks) {
+      const float4 x = *(const float4*)(part + (ks * M + m) * LD + n);
+      s.x += x.x;
+      s.y += x.y;
+      s.z += x.z;
+      s.w += x.w;
+    }
+    float4 r = base ? *(const float4*)(base + m * LD + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+    r.x = fmaf(sign, s.x, r.x);
+    r.y = fmaf(sign, s.y, r.y);
+    r.z = fmaf(sign, s.z, r.z);
+    r.w = fmaf(sign, s.w, r.w);
+    *(float4*)(out + m * LD + n) = r;
+  }
+}
+
+// out = sign * A B (or out += sign * A B when ACC) for a 16 x 16 matrix A
+// (row stride LS) and a 16 x 128 token tile B.
+template <bool ACC>
+__device__ __forceinline__ void small16(const float* A, const float* B, float* out, float sign) {
+  const int tid = threadIdx.x, ng = tid & 31, mg = tid >> 5;
+  float acc[2][4];
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) acc[m][t] = 0.0f;
+  gemm_acc<2, 4, true, true>(acc, A, LS, 2 * mg, B, LD, 4 * ng, 0, 0, C);
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    float4* o = (float4*)(out + (2 * mg + m) * LD + 4 * ng);
+    float4 r = ACC ? *o : make_float4(0.f, 0.f, 0.f, 0.f);
+    r.x = fmaf(sign, acc[m][0], r.x);
+    r.y = fmaf(sign, acc[m][1], r.y);
+    r.z = fmaf(sign, acc[m][2], r.z);
+    r.w = fmaf(sign, acc[m][3], r.w);
+    *o = r;
+  }
+}
+
+// sum_k X[m][k] Y[n][k] over the 128 channels of two token tiles.
+__device__ __forceinline__ float dot128(const float* X, int m, const float* Y, int n) {
+  float acc[1][1] = {{0.0f}};
+  gemm_acc<1, 1, true, false>(acc, X, LD, m, Y, LD, n, 0, 0, D);
+  return acc[0][0];
+}
+
+// The chunk's operands from q, k, theta (threads 0..127: one channel each,
+// sequential over the 16 tokens), v and beta (threads 128..255).  The decay
+// factors are running products of the per-token factors e^{g}: e^{G_t} =
+// prod_{s <= t} e^{g_s}, e^{-G_t} = prod_{s <= t} 1 / e^{g_s} and e^{G_C - G_t}
+// = prod_{s > t} e^{g_s}.  (The exponential of an fp32 cumulative sum would
+// carry the sum's rounding, up to half an ulp of |G| <= 80 per step, into
+// every factor; the products stay within a few ulp.)  Rows past the sequence
+// end are neutral (q = k = v = 0, g = 0, beta = 0).  Null outputs are skipped.
+// Kt is written times ksign; EGt receives e^{g}.
+template <typename Tin>
+__device__ __forceinline__ void load_chunk(const BwdDev& a, int64_t row0, int h, int nvalid,
+                                           float* Qt, float* Kt, float ksign, float* Kh,
+                                           float* KhC, float* EGt, float* dgt, float* ec,
+                                           float* bt, float* V) {
+  const int tid = threadIdx.x;
+  const Tin* q = (const Tin*)a.q;
+  const Tin* k = (const Tin*)a.k;
+  const Tin* th = (const Tin*)a.theta;
+  if (tid < D) {
+    const int c = tid;
+    // every load of the chunk first (independent, so they overlap), then the
+    // sequential pass over the tokens
+    float xr[C], kr[C], qr[C], egr[C];
+#pragma unroll
+    for (int t = 0; t < C; ++t) {
+      const bool ok = t < nvalid;
+      const int64_t idx = ((row0 + t) * a.H + h) * D + c;
+      xr[t] = ok ? to_f32(th[idx]) : 0.0f;
+      kr[t] = ok ? to_f32(k[idx]) : 0.0f;
+      qr[t] = (ok && Qt) ? to_f32(q[idx]) : 0.0f;
+    }
+    float E = 1.0f, Ei = 1.0f;
+#pragma unroll
+    for (int t = 0; t < C; ++t) {
+      const float kv = kr[t], qv = qr[t], x = xr[t];
+      float g = 0.0f, dg = 0.0f;
+      if (t < nvalid) {
+        if (a.log_decay) {
+          g = x;
+          dg = 1.0f;
+        } else {
+          // sigmoid(x) and sigmoid(-x) each from its own exponential: their
+          // product keeps full relative precision where one of them is near 1
+          const float sp = 1.0f / (1.0f + expf(-x)), sn = 1.0f / (1.0f + expf(x));
+          g = a.g_min * sp;
+          dg = a.g_min * sp * sn;
+        }
+      }
+      const float eg = expf(g);
+      E *= eg;
+      Ei *= 1.0f / eg;
+      egr[t] = eg;
+      Kt[t * LD + c] = ksign * kv * E;
+      Kh[t * LD + c] = kv * Ei;
+      if (Qt) Qt[t * LD + c] = qv * E;
+      if (EGt) EGt[t * LD + c] = eg;
+      if (dgt) dgt[t * LD + c] = dg;
+    }
+    ec[c] = E;
+    float P = 1.0f;
+#pragma unroll
+    for (int t = C - 1; t >= 0; --t) {
+      KhC[t * LD + c] = kr[t] * P;
+      P *= egr[t];
+    }
+  } else {
+    const int c = tid - D;
+    const Tin* v = (const Tin*)a.v;
+    const float b = (c < nvalid) ? to_f32(((const Tin*)a.beta)[(row0 + c) * a.H + h]) : 0.0f;
+    if (V) {
+      float vr[C];
+#pragma unroll
+      for (int t = 0; t < C; ++t)
+        vr[t] = t < nvalid ? to_f32(v[((row0 + t) * a.H + h) * D + c]) : 0.0f;
+#pragma unroll
+      for (int t = 0; t < C; ++t) V[t * LD + c] = vr[t];
+    }
+    if (c < C) bt[c] = b;
+  }
+}
+
+// 16 x 128 fp32 rows of d_out (zero past the sequence end).
+__device__ __forceinline__ void load_dout(const BwdDev& a, int64_t row0, int h, int nvalid,
+                                          float* dO) {
+  constexpr int kPer = C * D / kThreads;
+  float r[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = threadIdx.x + i * kThreads, t = e >> 7, c = e & (D - 1);
+    r[i] = t < nvalid ? a.d_out[((row0 + t) * a.H + h) * D + c] : 0.0f;
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = threadIdx.x + i * kThreads, t = e >> 7, c = e & (D - 1);
+    dO[t * LD + c] = r[i];
+  }
+}
+
+// M = (I + Diag(b) Ab)^{-1} by forward substitution (thread j < 16: column j),
+// Tb = M Diag(b), and the transpose of Tb when asked.
+__device__ __forceinline__ void wy_inverse(const float* Ab, const float* bt, float* M, float* Tb,
+                                           float* TbT) {
+  const int j = threadIdx.x;
+  if (j >= C) return;
+  float t[C];
+#pragma unroll
+  for (int i = 0; i < C; ++i) t[i] = (i == j) ? 1.0f : 0.0f;
+#pragma unroll
+  for (int i = 1; i < C; ++i) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int l = 0; l < i; ++l) acc = fmaf(Ab[i * LS + l], t[l], acc);
+    if (i > j) t[i] = -bt[i] * acc;
+  }
+  const float bj = bt[j];
+#pragma unroll
+  for (int i = 0; i < C; ++i) {
+    M[i * LS + j] = t[i];
+    Tb[i * LS + j] = t[i] * bj;
+    if (TbT) TbT[j * LS + i] = t[i] * bj;
+  }
+}
+
+// Thread tile of the register-resident 128 x 128 state: element [i][4 g + c]
+// is row 8 ig + i, column 64 g + 4 jg + c (ig = tid / 16, jg = tid % 16).
+__device__ __forceinline__ void state_store(const float (&st)[8][8], float* dst, int ld) {
+  const int ig = threadIdx.x >> 4, jg = threadIdx.x & 15;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+      *(float4*)(dst + (size_t)(8 * ig + i) * ld + 64 * g + 4 * jg) =
+          make_float4(st[i][4 * g], st[i][4 * g + 1], st[i][4 * g + 2], st[i][4 * g + 3]);
+}
+
+// The same tile from a dense 128 x 128 state in global memory (zero if null).
+__device__ __forceinline__ void state_load(float (&st)[8][8], const float* src) {
+  const int ig = threadIdx.x >> 4, jg = threadIdx.x & 15;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      const float4 x = src ? *(const float4*)(src + (size_t)(8 * ig + i) * D + 64 * g + 4 * jg)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      st[i][4 * g] = x.x;
+      st[i][4 * g + 1] = x.y;
+      st[i][4 * g + 2] = x.z;
+      st[i][4 * g + 3] = x.w;
+    }
+}
+
+// st <- Diag(ec) st + A^T B over K token rows (A, B row-major token tiles).
+template <int K>
+__device__ __forceinline__ void state_update(float (&st)[8][8], const float* ec, const float* A,
+                                             const float* B) {
+  const int ig = threadIdx.x >> 4, jg = threadIdx.x & 15;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float e = ec[8 * ig + i];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) st[i][j] *= e;
+  }
+  gemm_acc<8, 8, false, true>(st, A, LD, 8 * ig, B, LD, 4 * jg, 64, 0, K);
+}
+
+// ------------------------------------------------------------------ launch 1
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads, 1) kda_bwd_states_kernel(const BwdDev a) {
+  extern __shared__ __align__(16) float smf[];
+  float* S = smf;
+  float* Kt = S + STATE_F;
+  float* Kh = Kt + TILE_F;
+  float* KhC = Kh + TILE_F;
+  float* V = KhC + TILE_F;  // V, then R
+  float* U = V + TILE_F;
+  float* part = U + TILE_F;  // 4 tiles
+  float* Ab = part + 4 * TILE_F;
+  float* M = Ab + SM16_F;
+  float* Tb = M + SM16_F;
+  float* ec = Tb + SM16_F;
+  float* bt = ec + D;
+  const int tid = threadIdx.x;
+  const int64_t chain = blockIdx.x, b = chain / a.H;
+  const int h = (int)(chain - b * a.H);
+  float* Sw = a.ws_S + (size_t)chain * a.nch * kStateF;
+
+  float st[8][8];
+  state_load(st, a.init_state ? a.init_state + chain * kStateF : nullptr);
+  for (int n = 0; n < a.nch; ++n) {
+    state_store(st, Sw + (size_t)n * kStateF, D);
+    if (n + 1 == a.nch) break;  // the last chunk's end state is not needed
+    state_store(st, S, LD);
+    const int t0 = n * C, nvalid = min(C, a.T - t0);
+    const int64_t row0 = b * a.T + t0;
+    load_chunk<Tin>(a, row0, h, nvalid, nullptr, Kt, 1.0f, Kh, KhC, nullptr, nullptr, ec, bt, V);
+    __syncthreads();
+    {
+      const int m = tid >> 4, nn = tid & 15;
+      Ab[m * LS + nn] = nn < m ? dot128(Kt, m, Kh, nn) : 0.0f;
+    }
+    part16<true>(Kt, S, part);  // Kt S
+    __syncthreads();
+    wy_inverse(Ab, bt, M, Tb, nullptr);
+    reduce_parts<C, 4>(part, V, V, -1.0f);  // R = V - Kt S
+    __syncthreads();
+    small16<false>(Tb, V, U, 1.0f);  // U = Tb R
+    __syncthreads();
+    state_update<C>(st, ec, KhC, U);  // S' = Diag(ec) S + KhC^T U
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ launch 2
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads, 1) kda_bwd_reverse_kernel(const BwdDev a) {
+  extern __shared__ __align__(16) float smf[];
+  float* dS = smf;
+  float* Qt = dS + STATE_F;  // [Qt; -Kt]: 32 rows
+  float* mKt = Qt + TILE_F;
+  float* Kh = mKt + TILE_F;
+  float* KhC = Kh + TILE_F;
+  float* dO = KhC + TILE_F;  // [dO; dR]: 32 rows
+  float* dR = dO + TILE_F;
+  float* dU = dR + TILE_F;
+  float* part = dU + TILE_F;  // 4 tiles
+  float* Ab = part + 4 * TILE_F;
+  float* PiT = Ab + SM16_F;
+  float* M = PiT + SM16_F;
+  float* Tb = M + SM16_F;
+  float* TbT = Tb + SM16_F;
+  float* ec = TbT + SM16_F;
+  float* bt = ec + D;
+  const int tid = threadIdx.x;
+  const int64_t chain = blockIdx.x, b = chain / a.H;
+  const int h = (int)(chain - b * a.H);
+  float* dSw = a.ws_dS + (size_t)chain * a.nch * kStateF;
+  float* dUw = a.ws_dU + (size_t)chain * a.nch * C * D;
+
+  float st[8][8];
+  state_load(st, a.d_final ? a.d_final + chain * kStateF : nullptr);
+  for (int n = a.nch - 1; n >= 0; --n) {
+    state_store(st, dSw + (size_t)n * kStateF, D);
+    state_store(st, dS, LD);
+    const int t0 = n * C, nvalid = min(C, a.T - t0);
+    const int64_t row0 = b * a.T + t0;
+    load_chunk<Tin>(a, row0, h, nvalid, Qt, mKt, -1.0f, Kh, KhC, nullptr, nullptr, ec, bt, nullptr);
+    load_dout(a, row0, h, nvalid, dO);
+    __syncthreads();
+    {
+      const int m = tid >> 4, nn = tid & 15;
+      Ab[m * LS + nn] = nn < m ? -dot128(mKt, m, Kh, nn) : 0.0f;
+      PiT[nn * LS + m] = nn <= m ? dot128(Qt, m, Kh, nn) : 0.0f;
+    }
+    part16<true>(KhC, dS, part);  // KhC dS'
+    __syncthreads();
+    wy_inverse(Ab, bt, M, Tb, TbT);
+    small16<false>(PiT, dO, dU, 1.0f);  // Pi^T dO
+    __syncthreads();
+    reduce_parts<C, 4>(part, dU, dU, 1.0f);  // dU = Pi^T dO + KhC dS'
+    __syncthreads();
+    for (int e = tid; e < C * D / 4; e += kThreads) {
+      const int t = e >> 5, c = (e & 31) * 4;
+      *(float4*)(dUw + (size_t)n * C * D + t * D + c) = *(const float4*)(dU + t * LD + c);
+    }
+    small16<false>(TbT, dU, dR, 1.0f);  // dR = Tb^T dU
+    __syncthreads();
+    for (int e = tid; e < C * D; e += kThreads) {
+      const int t = e >> 7, c = e & (D - 1);
+      if (t < nvalid) a.dv[((row0 + t) * a.H + h) * D + c] = dR[t * LD + c];
+    }
+    state_update<2 * C>(st, ec, Qt, dO);  // dS = Diag(ec) dS' + [Qt; -Kt]^T [dO; dR]
+    __syncthreads();
+  }
+  if (a.d_init) state_store(st, a.d_init + chain * kStateF, D);
+}
+
+// ------------------------------------------------------------------ launch 3
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev a) {
+  extern __shared__ __align__(16) float smf[];
+  float* S = smf;  // S, then dS'
+  float* Qt = S + STATE_F;
+  float* Kt = Qt + TILE_F;
+  float* Kh = Kt + TILE_F;
+  float* KhC = Kh + TILE_F;
+  float* EGt = KhC + TILE_F;  // e^{g} per token and channel
+  float* dgt = EGt + TILE_F;
+  float* U = dgt + TILE_F;
+  float* X = U + TILE_F;  // [dO; -dR], then [dQt; dKt]
+  float* dKh = X + 2 * TILE_F;
+  float* V = dKh + TILE_F;  // V, then R, then row partials of dec
+  float* dU = V + TILE_F;   // dU, then dKhC
+  float* part = dU + TILE_F;  // 4 tiles
+  float* Ab = part + 4 * TILE_F;
+  float* Pi = Ab + SM16_F;
+  float* M = Pi + SM16_F;
+  float* Tb = M + SM16_F;
+  float* TbT = Tb + SM16_F;
+  float* dTb = TbT + SM16_F;  // dTb, then dA
+  float* dPi = dTb + SM16_F;
+  float* dPiT = dPi + SM16_F;
+  float* dAb = dPiT + SM16_F;
+  float* dAbT = dAb + SM16_F;
+  float* Y = dAbT + SM16_F;
+  float* ec = Y + SM16_F;
+  float* dec = ec + D;
+  float* bt = dec + D;
+  float* dbt = bt + C;
+  float* dpd = dbt + C;  // diagonal of dPi
+  const int tid = threadIdx.x, ig = tid >> 4, jg = tid & 15;
+  const int64_t chain = blockIdx.x / a.nch;
+  const int n = (int)(blockIdx.x - chain * a.nch);
+  const int64_t b = chain / a.H;
+  const int h = (int)(chain - b * a.H);
+  const int t0 = n * C, nvalid = min(C, a.T - t0);
+  const int64_t row0 = b * a.T + t0;
+  const size_t cidx = (size_t)chain * a.nch + n;
+  const float* Sg = a.ws_S + cidx * kStateF;
+  const float* dSg = a.ws_dS + cidx * kStateF;
+  const float* dUg = a.ws_dU + cidx * C * D;
+
+  // ---- operands of the chunk, S, dO and dU
+  load_chunk<Tin>(a, row0, h, nvalid, Qt, Kt, 1.0f, Kh, KhC, EGt, dgt, ec, bt, V);
+  load_dout(a, row0, h, nvalid, X);
+  {
+    float4 u[2], x[16];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int e = tid + i * kThreads;
+      u[i] = *(const float4*)(dUg + (e >> 5) * D + (e & 31) * 4);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int e = tid + i * kThreads;
+      x[i] = *(const float4*)(Sg + (size_t)(e >> 5) * D + (e & 31) * 4);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int e = tid + i * kThreads;
+      *(float4*)(dU + (e >> 5) * LD + (e & 31) * 4) = u[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int e = tid + i * kThreads;
+      *(float4*)(S + (e >> 5) * LD + (e & 31) * 4) = x[i];
+    }
   }
   __syncthreads();
+  {
+    const int m = tid >> 4, nn = tid & 15;
+    Ab[m * LS + nn] = nn < m ? dot128(Kt, m, Kh, nn) : 0.0f;
+    Pi[m * LS + nn] = nn <= m ? dot128(Qt, m, Kh, nn) : 0.0f;
+  }
+  part16<true>(Kt, S, part);  // Kt S
+  __syncthreads();
+  wy_inverse(Ab, bt, M, Tb, TbT);
+  reduce_parts<C, 4>(part, V, V, -1.0f);  // R = V - Kt S
+  __syncthreads();
+  small16<false>(Tb, V, U, 1.0f);              // U = Tb R
+  small16<false>(TbT, dU, X + TILE_F, -1.0f);  // -dR = -Tb^T dU
+  __syncthreads();
+  {
+    // dTb = lower_incl(dU R^T); dPi = lower_incl(dO U^T), its strictly lower
+    // part kept as a matrix and its diagonal apart (dpd): the diagonal of Pi is
+    // q_t . k_t, free of the decay, so its share of dq and dk is taken from q and
+    // k directly and it has no share in dG
+    const int m = tid >> 4, nn = tid & 15;
+    dTb[m * LS + nn] = nn <= m ? dot128(dU, m, V, nn) : 0.0f;
+    const float p = nn <= m ? dot128(X, m, U, nn) : 0.0f;
+    dPi[m * LS + nn] = nn < m ? p : 0.0f;
+    dPiT[nn * LS + m] = nn < m ? p : 0.0f;
+    if (nn == m) dpd[m] = p;
+  }
+  part32_nk(X, S, part);  // [dO; -dR] S^T
+  __syncthreads();
+  {
+    // Y = (dTb Diag(b)) M^T; db (first part) = column sums of M * dTb
+    const int i = tid >> 4, j = tid & 15;
+    float y = 0.0f;
+#pragma unroll
+    for (int l = 0; l < C; ++l) y = fmaf(dTb[i * LS + l] * bt[l], M[j * LS + l], y);
+    Y[i * LS + j] = y;
+    if (tid < C) {
+      float s = 0.0f;
+#pragma unroll
+      for (int r = 0; r < C; ++r) s = fmaf(M[r * LS + tid], dTb[r * LS + tid], s);
+      dbt[tid] = s;
+    }
+  }
+  reduce_parts<2 * C, 2>(part, X, nullptr, 1.0f);  // [dQt; dKt], the S^T parts
+  float d[8][8];
+  {
+    // dec_i = sum_j dS'_ij S_ij: row partials of this thread's tile
+    state_load(d, dSg);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float s = 0.0f;
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          s = fmaf(d[i][4 * g + c], S[(8 * ig + i) * LD + 64 * g + 4 * jg + c], s);
+      V[jg * LD + 8 * ig + i] = s;
+    }
+  }
+  __syncthreads();
+  state_store(d, S, LD);  // S is no longer needed: dS' takes its place
+  {
+    // dA = -strict_lower(M^T Y) (kept in dTb's place), dAb = Diag(b) dA
+    const int i = tid >> 4, j = tid & 15;
+    float s = 0.0f;
+#pragma unroll
+    for (int l = 0; l < C; ++l) s = fmaf(M[l * LS + i], Y[l * LS + j], s);
+    const float dA = i > j ? -s : 0.0f;
+    dTb[i * LS + j] = dA;
+    dAb[i * LS + j] = bt[i] * dA;
+    dAbT[j * LS + i] = bt[i] * dA;
+  }
   if (tid < D) {
     float s = 0.0f;
 #pragma unroll
-    for (int i = 0; i < NT; ++i) s += sh.colp[i][tid];
-    sh.vec[0][tid] = sh.beta * (sh.v[tid] - s);  // u
+    for (int r = 0; r < 16; ++r) s += V[r * LD + tid];
+    dec[tid] = s;
   }
   __syncthreads();
+  part16<false>(U, S, part);  // U dS'^T
+  if (tid < C) {
+    float s = dbt[tid];
 #pragma unroll
-  for (int a = 0; a < TT; ++a)
+    for (int l = 0; l < C; ++l) s = fmaf(dTb[tid * LS + l], Ab[tid * LS + l], s);
+    dbt[tid] = s;
+  }
+  small16<true>(dPi, Kh, X, 1.0f);           // dQt += dPi Kh (strictly lower dPi)
+  small16<true>(dAb, Kh, X + TILE_F, 1.0f);  // dKt += Diag(b) dA Kh
+  small16<false>(dPiT, Qt, dKh, 1.0f);       // dKh = dPi^T Qt (strictly lower dPi)
+  __syncthreads();
+  small16<true>(dAbT, Kt, dKh, 1.0f);           // dKh += (Diag(b) dA)^T Kt
+  reduce_parts<C, 4>(part, dU, nullptr, 1.0f);  // dKhC
+  __syncthreads();
+  // ---- per channel: dK, dQ, dG and the reverse cumulative sum.  The KhC
+  // terms enter dg_s as -sum_{t >= s} dKhC_t KhC_t (through dG_t) plus
+  // sum_t dKhC_t KhC_t (through dG_C); they are summed in the equal closed
+  // form sum_{t < s} dKhC_t KhC_t, which avoids cancelling two large sums when
+  // the last tokens' terms dominate (fast decay).
+  if (tid < D) {
+    const int c = tid;
+    // the decay factors again, by the same products as in load_chunk
+    float sfx[C];  // e^{G_C - G_t}
+    float P = 1.0f;
 #pragma unroll
-    for (int b = 0; b < TT; ++b) S[a][b] = fmaf(sh.k[TT * r + a], sh.vec[0][TT * c + b], S[a][b]);
-}
-
-__device__ __forceinline__ void load_tile(float (&S)[TT][TT], const float* src, int r, int c) {
+    for (int t = C - 1; t >= 0; --t) {
+      sfx[t] = P;
+      P *= EGt[t * LD + c];
+    }
+    float qr[C], kr[C];
 #pragma unroll
-  for (int a = 0; a < TT; ++a) {
-    const float4* p = (const float4*)(src + (size_t)(TT * r + a) * D + TT * c);
-    const float4 x = p[0], y = p[1];
-    S[a][0] = x.x; S[a][1] = x.y; S[a][2] = x.z; S[a][3] = x.w;
-    S[a][4] = y.x; S[a][5] = y.y; S[a][6] = y.z; S[a][7] = y.w;
+    for (int t = 0; t < C; ++t) {
+      const int64_t o = ((row0 + t) * a.H + h) * D + c;
+      qr[t] = t < nvalid ? to_f32(((const Tin*)a.q)[o]) : 0.0f;
+      kr[t] = t < nvalid ? to_f32(((const Tin*)a.k)[o]) : 0.0f;
+    }
+    float E = 1.0f, Ei = 1.0f;
+    float dG[C], pre[C];
+    float run = 0.0f;
+#pragma unroll
+    for (int t = 0; t < C; ++t) {
+      const float eg = EGt[t * LD + c];
+      E *= eg;
+      Ei *= 1.0f / eg;
+      const float dqt = X[t * LD + c], dkt = X[(C + t) * LD + c];
+      const float dkh = dKh[t * LD + c], dkhc = dU[t * LD + c];
+      dG[t] = dkt * Kt[t * LD + c] + dqt * Qt[t * LD + c] - dkh * Kh[t * LD + c];
+      pre[t] = run;  // sum_{u < t} dKhC_u KhC_u
+      run = fmaf(dkhc, KhC[t * LD + c], run);
+      if (t < nvalid) {
+        const int64_t o = ((row0 + t) * a.H + h) * D + c;
+        a.dq[o] = fmaf(dpd[t], kr[t], dqt * E);
+        a.dk[o] = fmaf(dpd[t], qr[t], dkt * E + dkh * Ei + dkhc * sfx[t]);
+      }
+    }
+    const float dec_ec = dec[c] * ec[c];
+    float acc = 0.0f;
+#pragma unroll
+    for (int t = C - 1; t >= 0; --t) {
+      acc += dG[t];
+      if (t < nvalid)
+        a.dtheta[((row0 + t) * a.H + h) * D + c] = (acc + pre[t] + dec_ec) * dgt[t * LD + c];
+    }
+  } else if (tid - D < nvalid) {
+    a.dbeta[(row0 + tid - D) * a.H + h] = dbt[tid - D];
   }
 }
 
-__device__ __forceinline__ void store_tile(const float (&S)[TT][TT], float* dst, int r, int c) {
-#pragma unroll
-  for (int a = 0; a < TT; ++a) {
-    float4* p = (float4*)(dst + (size_t)(TT * r + a) * D + TT * c);
-    p[0] = make_float4(S[a][0], S[a][1], S[a][2], S[a][3]);
-    p[1] = make_float4(S[a][4], S[a][5], S[a][6], S[a][7]);
-  }
-}
+constexpr size_t kSmemStates = (size_t)(STATE_F + 9 * TILE_F + 3 * SM16_F + D + C) * 4;
+constexpr size_t kSmemReverse = (size_t)(STATE_F + 11 * TILE_F + 5 * SM16_F + D + C) * 4;
+constexpr size_t kSmemGrads = (size_t)(STATE_F + 16 * TILE_F + 11 * SM16_F + 2 * D + 3 * C) * 4;
+static_assert(kSmemGrads <= 232448 && kSmemReverse <= 232448, "shared memory budget");
 
 template <typename Tin>
-__global__ void __launch_bounds__(kThreads, 1)
-    kda_bwd_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
-                   const Tin* __restrict__ theta, const Tin* __restrict__ beta, float g_min, int gate,
-                   const float* __restrict__ init_state, const float* __restrict__ d_out,
-                   const float* __restrict__ d_final, float* __restrict__ dq,
-                   float* __restrict__ dk, float* __restrict__ dv, float* __restrict__ dtheta,
-                   float* __restrict__ dbeta, float* __restrict__ d_init, float* __restrict__ ws,
-                   int H, int T) {
-  __shared__ BwdShared sh;
-  const int tid = threadIdx.x, r = tid / NT, c = tid % NT;
-  const int64_t chain = blockIdx.x;  // sequence * H + head
-  const int64_t b = chain / H, h = chain - b * H;
-  const int nblk = (T + kBlock - 1) / kBlock;
-  float* ckpt = ws + (size_t)chain * (size_t)(nblk + kBlock) * kState;  // nblk states
-  float* blk = ckpt + (size_t)nblk * kState;                            // kBlock states
-  auto row_of = [&](int t) { return (b * T + t) * H + h; };
-
-  // ---- forward pass: the state at the start of every block
-  float S[TT][TT];
-  if (init_state)
-    load_tile(S, init_state + chain * kState, r, c);
-  else
-#pragma unroll
-    for (int a = 0; a < TT; ++a)
-#pragma unroll
-      for (int bb = 0; bb < TT; ++bb) S[a][bb] = 0.0f;
-  for (int t = 0; t < T; ++t) {
-    if (t % kBlock == 0) store_tile(S, ckpt + (size_t)(t / kBlock) * kState, r, c);
-    __syncthreads();
-    load_token(sh, q, k, v, theta, beta, d_out, row_of(t), g_min, gate, tid);
-    __syncthreads();
-    fwd_step(sh, S, r, c, tid);
-  }
-
-  // ---- reverse pass
-  float L[TT][TT];
-  if (d_final)
-    load_tile(L, d_final + chain * kState, r, c);
-  else
-#pragma unroll
-    for (int a = 0; a < TT; ++a)
-#pragma unroll
-      for (int bb = 0; bb < TT; ++bb) L[a][bb] = 0.0f;
-  for (int blkI = nblk - 1; blkI >= 0; --blkI) {
-    const int t0 = blkI * kBlock, t1 = min(T, t0 + kBlock);
-    // the states before each token of the block
-    __syncthreads();
-    load_tile(S, ckpt + (size_t)blkI * kState, r, c);
-    for (int t = t0; t < t1; ++t) {
-      store_tile(S, blk + (size_t)(t - t0) * kState, r, c);
-      __syncthreads();
-      load_token(sh, q, k, v, theta, beta, d_out, row_of(t), g_min, gate, tid);
-      __syncthreads();
-      fwd_step(sh, S, r, c, tid);
-    }
-    __syncthreads();
-    for (int t = t1 - 1; t >= t0; --t) {
-      load_token(sh, q, k, v, theta, beta, d_out, row_of(t), g_min, gate, tid);
-      __syncthreads();
-      float X[TT][TT];
-      load_tile(X, blk + (size_t)(t - t0) * kState, r, c);
-#pragma unroll
-      for (int a = 0; a < TT; ++a)
-#pragma unroll
-        for (int bb = 0; bb < TT; ++bb) X[a][bb] *= sh.e[TT * r + a];
-      // column sums: k^T X and (with L += q do^T first) k^T L
-#pragma unroll
-      for (int a = 0; a < TT; ++a)
-#pragma unroll
-        for (int bb = 0; bb < TT; ++bb)
-          L[a][bb] = fmaf(sh.q[TT * r + a], sh.dout[TT * c + bb], L[a][bb]);
-#pragma unroll
-      for (int bb = 0; bb < TT; ++bb) {
-        float px = 0.0f, pl = 0.0f;
-#pragma unroll
-        for (int a = 0; a < TT; ++a) {
-          px = fmaf(sh.k[TT * r + a], X[a][bb], px);
-          pl = fmaf(sh.k[TT * r + a], L[a][bb], pl);
-        }
-        sh.colp[r][TT * c + bb] = px;
-        sh.rowp[r][TT * c + bb] = pl;  // (a second column-sum buffer)
-      }
-      __syncthreads();
-      if (tid < D) {
-        float sx = 0.0f, sl = 0.0f;
-#pragma unroll
-        for (int i = 0; i < NT; ++i) {
-          sx += sh.colp[i][tid];
-          sl += sh.rowp[i][tid];
-        }
-        const float w = sh.v[tid] - sx;        // v - X^T k
-        sh.vec[0][tid] = sh.beta * w;          // u
-        sh.vec[1][tid] = sl;                   // kL = L^T k
-        sh.vec[2][tid] = sl * w;               // terms of dbeta
-        dv[row_of(t) * D + tid] = sh.beta * sl;
-      }
-      __syncthreads();
-      // row sums: dq = S_t do = X do + k (u . do); dk = L u - beta X kL;
-      // dg = sum_j dX_ij X_ij with dX = L - beta k kL^T
-#pragma unroll
-      for (int a = 0; a < TT; ++a) {
-        float pq = 0.0f, pk = 0.0f, pg = 0.0f;
-        const float ki = sh.k[TT * r + a];
-#pragma unroll
-        for (int bb = 0; bb < TT; ++bb) {
-          const int j = TT * c + bb;
-          const float u = sh.vec[0][j], kl = sh.vec[1][j], dO = sh.dout[j];
-          const float st = fmaf(ki, u, X[a][bb]);  // S_t
-          pq = fmaf(st, dO, pq);
-          pk = fmaf(L[a][bb], u, pk);
-          pk = fmaf(-sh.beta * X[a][bb], kl, pk);
-          const float dX = fmaf(-sh.beta * ki, kl, L[a][bb]);
-          pg = fmaf(dX, X[a][bb], pg);
-          L[a][bb] = sh.e[TT * r + a] * dX;  // gradient w.r.t. S_{t-1}
-        }
-        sh.colp[c][TT * r + a] = pq;  // row partials, indexed [tile column][row]
-        sh.rowp[c][TT * r + a] = pk;
-        X[a][0] = pg;                 // the dg partial of row a (X[a][.] is done)
-      }
-      __syncthreads();
-      if (tid < D) {
-        float sq = 0.0f, sk = 0.0f;
-#pragma unroll
-        for (int i = 0; i < NT; ++i) {
-          sq += sh.colp[i][tid];
-          sk += sh.rowp[i][tid];
-        }
-        const int64_t o = row_of(t) * D + tid;
-        dq[o] = sq;
-        dk[o] = sk;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int a = 0; a < TT; ++a) sh.colp[c][TT * r + a] = X[a][0];
-      __syncthreads();
-      if (tid < D) {
-        float sg = 0.0f;
-#pragma unroll
-        for (int i = 0; i < NT; ++i) sg += sh.colp[i][tid];
-        dtheta[row_of(t) * D + tid] = sg * sh.dgate[tid];
-      }
-      if (tid >= D && tid < D + 32) {
-        // dbeta = sum_j kL_j (v_j - X^T k)_j: one warp
-        const int l = tid - D;
-        float s = 0.0f;
-        for (int j = l; j < D; j += 32) s += sh.vec[2][j];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (l == 0) dbeta[row_of(t)] = s;
-      }
-      __syncthreads();
-    }
-  }
-  if (d_init) store_tile(L, d_init + chain * kState, r, c);
+int launch_bwd_t(const BwdDev& d, int64_t chains, cudaStream_t stream) {
+  const void* fns[3] = {(const void*)kda_bwd_states_kernel<Tin>,
+                        (const void*)kda_bwd_reverse_kernel<Tin>,
+                        (const void*)kda_bwd_grads_kernel<Tin>};
+  const size_t smem[3] = {kSmemStates, kSmemReverse, kSmemGrads};
+  for (int i = 0; i < 3; ++i)
+    if (cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem[i]) !=
+        cudaSuccess)
+      return KDA_ERR_LAUNCH;
+  kda_bwd_states_kernel<Tin><<<(unsigned)chains, kThreads, kSmemStates, stream>>>(d);
+  kda_bwd_reverse_kernel<Tin><<<(unsigned)chains, kThreads, kSmemReverse, stream>>>(d);
+  kda_bwd_grads_kernel<Tin><<<(unsigned)(chains * d.nch), kThreads, kSmemGrads, stream>>>(d);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
 }  // namespace
 
 size_t bwd_workspace_size(int B, int H, int T) {
-  const int nblk = (T + kBlock - 1) / kBlock;
-  return (size_t)B * H * (size_t)(nblk + kBlock) * kState * sizeof(float);
+  const size_t nch = ((size_t)T + C - 1) / C;
+  return (size_t)B * H * nch * (2 * kStateF + (size_t)C * D) * sizeof(float);
 }
 
 // (dk = dv = 128 is checked by the caller)
 int launch_bwd(const BwdParams& p, cudaStream_t stream) {
-  const unsigned grid = (unsigned)((int64_t)p.B * p.H);
-  if (grid == 0 || p.T == 0) return KDA_OK;
-  if (p.dtype == KDA_DTYPE_F32) {
-    kda_bwd_kernel<float><<<grid, kThreads, 0, stream>>>(
-        (const float*)p.q, (const float*)p.k, (const float*)p.v, (const float*)p.theta,
-        (const float*)p.beta, p.g_min, p.gate, p.init_state, p.d_out, p.d_final, p.dq, p.dk, p.dv,
-        p.dtheta, p.dbeta, p.d_init, (float*)p.workspace, p.H, p.T);
-  } else {
-    kda_bwd_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
-        (const __nv_bfloat16*)p.q, (const __nv_bfloat16*)p.k, (const __nv_bfloat16*)p.v,
-        (const __nv_bfloat16*)p.theta, (const __nv_bfloat16*)p.beta, p.g_min, p.gate, p.init_state,
-        p.d_out, p.d_final, p.dq, p.dk, p.dv, p.dtheta, p.dbeta, p.d_init, (float*)p.workspace, p.H,
-        p.T);
-  }
-  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+  const int64_t chains = (int64_t)p.B * p.H;
+  if (chains == 0 || p.T == 0) return KDA_OK;
+  const int nch = (p.T + C - 1) / C;
+  if (chains * nch > (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
+  BwdDev d;
+  d.q = p.q;
+  d.k = p.k;
+  d.v = p.v;
+  d.theta = p.theta;
+  d.beta = p.beta;
+  d.g_min = p.g_min;
+  d.log_decay = p.gate == KDA_GATE_LOG_DECAY;
+  d.init_state = p.init_state;
+  d.d_out = p.d_out;
+  d.d_final = p.d_final;
+  d.dq = p.dq;
+  d.dk = p.dk;
+  d.dv = p.dv;
+  d.dtheta = p.dtheta;
+  d.dbeta = p.dbeta;
+  d.d_init = p.d_init;
+  d.ws_S = (float*)p.workspace;
+  d.ws_dS = d.ws_S + (size_t)chains * nch * kStateF;
+  d.ws_dU = d.ws_dS + (size_t)chains * nch * kStateF;
+  d.H = p.H;
+  d.T = p.T;
+  d.nch = nch;
+  if (p.dtype == KDA_DTYPE_F32) return launch_bwd_t<float>(d, chains, stream);
+  return launch_bwd_t<__nv_bfloat16>(d, chains, stream);
 }
 
 }  // namespace kda

@@ -225,7 +225,7 @@ def kda_chunk_fwd_segmented(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
               DTYPES[q.dtype], DTYPES[out_dtype], PATHS["mma"])
     with torch.cuda.device(q.device):
         rc = lib.kda_chunk_fwd_segmented(ctypes.byref(a), int(segments), _ptr(workspace),
-                                         workspace.numel(), _stream_ptr(stream))
+                                         workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd_segmented")
     return out, final_state
@@ -286,8 +286,8 @@ def kda_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torc
                  _ptr(g["dv"]), _ptr(g["dtheta"]), _ptr(g["dbeta"]), _ptr(g["d_init"]),
                  B, H, T, dk, dv, DTYPES[q.dtype], GATES[gate])
     with torch.cuda.device(dev):
-        rc = lib.kda_chunk_bwd(ctypes.byref(a), _ptr(workspace), workspace.numel(),
-                               _stream_ptr(stream))
+        rc = lib.kda_chunk_bwd(ctypes.byref(a), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_chunk_bwd")
     return g

@@ -54,3 +54,28 @@ def test_bwd_log_decay_gate_and_no_state_gradients():
     for name, key in (("dq", "dq"), ("dk", "dk"), ("dv", "dv"), ("dtheta", "dtheta"),
                       ("dbeta", "dbeta"), ("d_init", "dS0")):
         assert_close(f64(got[name]), ref[key], TOL_BWD, f"{name} (log-decay gate)")
+
+
+def test_bwd_fast_decay_multi_chain():
+    """theta ~ U[6, 12] (every log-decay near g_min, sigmoid(theta) near 1),
+    beta ~ U[0.9, 1], B = 2, H = 3, T = 48 (three whole chunks): chain
+    indexing of every launch and the gate derivative where 1 - sigmoid is
+    small."""
+    B, H, T = 2, 3, 48
+    w = Workload("bwd_fast", B=B, H=H, T=T, dk=128, dv=128, dtype=torch.bfloat16,
+                 theta="uniform6_12", beta="uniform09_1", init_std=0.05)
+    inp = make_inputs(w, seed=5)
+    g = torch.Generator().manual_seed(6)
+    d_out = torch.randn(B, T, H, 128, generator=g)
+    d_fin = torch.randn(B, H, 128, 128, generator=g)
+    ref = backward.bwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["theta"]),
+                       f64(inp["beta"]), -5.0, f64(inp["init_state"]), d_out.double().numpy(),
+                       d_fin.double().numpy())
+    c = lambda x: x.cuda()
+    got = kda_chunk_bwd(c(inp["q"]), c(inp["k"]), c(inp["v"]), c(inp["theta"]), c(inp["beta"]),
+                        c(d_out), -5.0, c(inp["init_state"]), c(d_fin))
+    torch.cuda.synchronize()
+    assert kda_device_status(clear=True) == 0
+    for name, key in (("dq", "dq"), ("dk", "dk"), ("dv", "dv"), ("dtheta", "dtheta"),
+                      ("dbeta", "dbeta"), ("d_init", "dS0")):
+        assert_close(f64(got[name]), ref[key], TOL_BWD, f"{name} fast decay")
