@@ -82,9 +82,26 @@ def measured_peaks() -> tuple[dict, str]:
             "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_source_hash() -> str:
+# The files each profiled kernel is compiled from (its translation unit and the
+# headers it includes); other kernels' sources do not invalidate its capture.
+KERNEL_SOURCES = {
+    "kda_fwd_mma_kernel": ["csrc/kda_mma.cu", "csrc/kda_tmap.cu", "csrc/kda_sm100.cuh",
+                           "csrc/kda_device.cuh", "csrc/kda_internal.cuh"],
+    "kda_fwd_tc_kernel": ["csrc/kda_tc.cu", "csrc/kda_tmap.cu", "csrc/kda_sm100.cuh",
+                          "csrc/kda_device.cuh", "csrc/kda_internal.cuh"],
+    "kda_decode_kernel": ["csrc/kda_decode.cu", "csrc/kda_device.cuh", "csrc/kda_internal.cuh"],
+    "kda_bwd": ["csrc/kda_bwd.cu", "csrc/kda_device.cuh", "csrc/kda_internal.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str = "") -> str:
+    """Hash of the sources of `kernel` (every CUDA source for an unknown name)."""
+    pkg = os.path.join(ROOT, "linear_attention_04_gb300")
+    files = KERNEL_SOURCES.get(kernel)
+    paths = ([os.path.join(pkg, f) for f in files] if files else
+             glob.glob(os.path.join(pkg, "csrc", "*")))
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "linear_attention_04_gb300", "csrc", "*"))):
+    for f in sorted(paths):
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -93,7 +110,7 @@ def kernel_source_hash() -> str:
 def traffic_from_profiles(kernel: str, workload: str) -> tuple[int | None, str | None]:
     """DRAM bytes per launch recorded from an ncu capture under profiles/, if
     the kernel sources still hash to the value recorded with it."""
-    want = kernel_source_hash()
+    want = kernel_source_hash(kernel)
     for f in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.txt")) +
                     glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         kv = {}
@@ -543,6 +560,21 @@ def run_decode(args, rank, world, local):
 
 # ----------------------------------------------------------------------------- backward
 
+# fp32 CUDA-core peak of one GB300: 152 SMs x 128 fp32 FMA lanes x 2 flop x 2070 MHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def bwd_flops(w, inp, C=16) -> int:
+    """Algorithmic FLOPs of one chunked backward pass: per token-head
+    2 (9 d^2 + d^2 / C + 16 C d + 2 C^2) at d = dk = dv -- the chunk products of
+    the three launches (states: Kt S, KhC^T U and the 16 x 16 products; reverse:
+    KhC dS', [Qt; -Kt]^T [dO; dR] and the 16 x 16 products; gradients: Kt S,
+    [dO; -dR] S^T, U dS'^T, dS' * S and the 16 x 16 products)."""
+    d = w.dk
+    n = n_tokens(inp) * w.H
+    return n * 2 * (9 * d * d + d * d // C + 16 * C * d + 2 * C * C)
+
+
 def bwd_bytes(w, inp, e=2) -> int:
     """HBM bytes of one backward pass (token-heads x per-token-head bytes): the
     bf16 inputs, the fp32 d_out, the fp32 gradients dq, dk, dtheta, dv, dbeta."""
@@ -587,7 +619,9 @@ def run_bwd(args, rank, world, local):
     step_s = total_ms / args.steps / 1e3
     peaks, peak_src = measured_peaks()
     nbytes = bwd_bytes(w, inp)
-    achieved = nbytes / step_s / 1e9
+    flops = bwd_flops(w, inp)
+    achieved = flops / step_s / 1e12
+    traffic, traffic_src = traffic_from_profiles("kda_bwd", w.name)
     tokens = n_tokens(inp)
     return {"metric": "KDA backward tokens/s (all gradients of the forward pass)",
             "value": tokens * world / step_s, "unit": "tokens/s", "n_gpus": world,
@@ -597,10 +631,16 @@ def run_bwd(args, rank, world, local):
             "op": "bwd",
             "config": {"workload": f"{w.name}: B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv}, "
                                    "fp32 arithmetic on CUDA cores"},
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 5),
-                         "traffic": None, "peak_source": f"hbm_gbs of {peak_src}",
-                         "kernel": "kda_bwd_kernel", "algorithmic_bytes_per_launch": nbytes},
+            "roofline": {"bound": "alu", "achieved": round(achieved, 2),
+                         "peak": round(FP32_ALU_TFLOPS, 1), "unit": "TFLOP/s",
+                         "frac": round(achieved / FP32_ALU_TFLOPS, 4), "traffic": traffic,
+                         "traffic_source": traffic_src,
+                         "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 x 2070 MHz",
+                         "kernel": "kda_bwd_states + kda_bwd_reverse + kda_bwd_grads (one pass)",
+                         "algorithmic_flops_per_pass": flops,
+                         "hbm": {"achieved_gbs": round(nbytes / step_s / 1e9, 1),
+                                 "peak_gbs": peaks["hbm_gbs"],
+                                 "algorithmic_bytes_per_pass": nbytes}},
             "cpu_baseline": None, "e2e": None, "gpu_launches": args.steps}
 
 

@@ -183,9 +183,10 @@ KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* args, int segments, void
  * kda_chunk_bwd -- gradients of kda_chunk_fwd's outputs and final state with
  * respect to q, k, v, theta, beta and the initial state (the reverse pass of
  * the recurrence of "Kimi K3 Deep Dive", section "Core Innovation 1"), in fp32
- * on CUDA cores.  A correctness-first path: token-level reverse recursion,
- * with the states before each token recomputed from block checkpoints in the
- * caller's workspace.
+ * on CUDA cores, in chunked (WY) form: a forward pass that stores the state at
+ * every 16-token chunk start, a reverse pass that carries the state gradient
+ * and stores it at every chunk end, and one parallel pass over all chunks for
+ * the remaining gradients (three kernel launches on `stream`).
  * Requires dk = dv = 128 and a fixed-length batch.  Layouts as kda_chunk_fwd:
  * q, k, theta, dq, dk, dtheta [B,T,H,dk]; v, d_out, dv [B,T,H,dv]; beta,
  * dbeta [B,T,H]; init_state, d_final, d_init [B,H,dk,dv] fp32 (each of the
@@ -193,8 +194,12 @@ KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* args, int segments, void
  * written).  `dtype` (KDA_DTYPE_*) is the type of q, k, v, theta, beta; every
  * gradient and d_out/d_final are fp32.  `gate` as kda_fwd_args.gate.
  * `workspace`: device memory of kda_chunk_bwd_workspace_size(B, H, T, dk, dv)
- * bytes, 16-byte aligned, caller-owned, scratch until the stream has passed
- * the call.  The library allocates nothing.  Returns KDA_OK or KDA_ERR_*.
+ * bytes (B * H * ceil(T / 16) * 136 KB: two fp32 128 x 128 states and a
+ * 16 x 128 fp32 tile per chunk), 16-byte aligned, caller-owned, scratch until
+ * the stream has passed the call; it needs no initial contents.  The library
+ * allocates nothing.  A given log-decay (KDA_GATE_LOG_DECAY) has the forward
+ * pass's limit: the in-chunk sum of |g| below about 88.  Returns KDA_OK or
+ * KDA_ERR_*.
  */
 typedef struct kda_bwd_args {
   const void* q;
