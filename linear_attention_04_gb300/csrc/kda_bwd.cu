@@ -240,23 +240,24 @@ __device__ __forceinline__ float dot128(const float* X, int m, const float* Y, i
 }
 
 // The chunk's operands from q, k, theta (threads 0..127: one channel each,
-// sequential over the 16 tokens), v and beta (threads 128..255).  The decay
-// factors are running products of the per-token factors e^{g}: e^{G_t} =
-// prod_{s <= t} e^{g_s}, e^{-G_t} = prod_{s <= t} 1 / e^{g_s} and e^{G_C - G_t}
-// = prod_{s > t} e^{g_s}.  (The exponential of an fp32 cumulative sum would
+// sequential over the 16 tokens), v and beta (threads 128..255).  Element
+// (t, c) of theta is th0[t * rs + c], and so on for k, q and v: rows of the
+// global tensors (rs = H * D) or of a staged copy in shared memory (rs = D).
+// Thread 128 + t (t < 16) passes beta_t in bval.  The decay factors are
+// running products of the per-token factors e^{g}: e^{G_t} = prod_{s <= t}
+// e^{g_s}, e^{-G_t} = prod_{s <= t} 1 / e^{g_s} and e^{G_C - G_t} =
+// prod_{s > t} e^{g_s}.  (The exponential of an fp32 cumulative sum would
 // carry the sum's rounding, up to half an ulp of |G| <= 80 per step, into
 // every factor; the products stay within a few ulp.)  Rows past the sequence
-// end are neutral (q = k = v = 0, g = 0, beta = 0).  Null outputs are skipped.
-// Kt is written times ksign; EGt receives e^{g}.
+// end are neutral (q = k = v = 0, g = 0, beta = 0).  Null outputs are
+// skipped.  Kt is written times ksign; EGt receives e^{g}.
 template <typename Tin>
-__device__ __forceinline__ void load_chunk(const BwdDev& a, int64_t row0, int h, int nvalid,
-                                           float* Qt, float* Kt, float ksign, float* Kh,
-                                           float* KhC, float* EGt, float* dgt, float* ec,
-                                           float* bt, float* V) {
+__device__ __forceinline__ void load_chunk(const Tin* th0, const Tin* k0, const Tin* q0,
+                                           const Tin* v0, int64_t rs, float bval, float g_min,
+                                           int log_decay, int nvalid, float* Qt, float* Kt,
+                                           float ksign, float* Kh, float* KhC, float* EGt,
+                                           float* dgt, float* ec, float* bt, float* V) {
   const int tid = threadIdx.x;
-  const Tin* q = (const Tin*)a.q;
-  const Tin* k = (const Tin*)a.k;
-  const Tin* th = (const Tin*)a.theta;
   if (tid < D) {
     const int c = tid;
     // every load of the chunk first (independent, so they overlap), then the
@@ -265,10 +266,9 @@ __device__ __forceinline__ void load_chunk(const BwdDev& a, int64_t row0, int h,
 #pragma unroll
     for (int t = 0; t < C; ++t) {
       const bool ok = t < nvalid;
-      const int64_t idx = ((row0 + t) * a.H + h) * D + c;
-      xr[t] = ok ? to_f32(th[idx]) : 0.0f;
-      kr[t] = ok ? to_f32(k[idx]) : 0.0f;
-      qr[t] = (ok && Qt) ? to_f32(q[idx]) : 0.0f;
+      xr[t] = ok ? to_f32(th0[t * rs + c]) : 0.0f;
+      kr[t] = ok ? to_f32(k0[t * rs + c]) : 0.0f;
+      qr[t] = (ok && Qt) ? to_f32(q0[t * rs + c]) : 0.0f;
     }
     float E = 1.0f, Ei = 1.0f;
 #pragma unroll
@@ -276,15 +276,15 @@ __device__ __forceinline__ void load_chunk(const BwdDev& a, int64_t row0, int h,
       const float kv = kr[t], qv = qr[t], x = xr[t];
       float g = 0.0f, dg = 0.0f;
       if (t < nvalid) {
-        if (a.log_decay) {
+        if (log_decay) {
           g = x;
           dg = 1.0f;
         } else {
           // sigmoid(x) and sigmoid(-x) each from its own exponential: their
           // product keeps full relative precision where one of them is near 1
           const float sp = 1.0f / (1.0f + expf(-x)), sn = 1.0f / (1.0f + expf(x));
-          g = a.g_min * sp;
-          dg = a.g_min * sp * sn;
+          g = g_min * sp;
+          dg = g_min * sp * sn;
         }
       }
       const float eg = expf(g);
@@ -306,17 +306,47 @@ __device__ __forceinline__ void load_chunk(const BwdDev& a, int64_t row0, int h,
     }
   } else {
     const int c = tid - D;
-    const Tin* v = (const Tin*)a.v;
-    const float b = (c < nvalid) ? to_f32(((const Tin*)a.beta)[(row0 + c) * a.H + h]) : 0.0f;
     if (V) {
       float vr[C];
 #pragma unroll
-      for (int t = 0; t < C; ++t)
-        vr[t] = t < nvalid ? to_f32(v[((row0 + t) * a.H + h) * D + c]) : 0.0f;
+      for (int t = 0; t < C; ++t) vr[t] = t < nvalid ? to_f32(v0[t * rs + c]) : 0.0f;
 #pragma unroll
       for (int t = 0; t < C; ++t) V[t * LD + c] = vr[t];
     }
-    if (c < C) bt[c] = b;
+    if (c < C) bt[c] = bval;
+  }
+}
+
+// beta_t of the chunk for thread 128 + t (t < 16), zero elsewhere.
+template <typename Tin>
+__device__ __forceinline__ float load_beta(const BwdDev& a, int64_t row0, int h, int nvalid) {
+  const int t = (int)threadIdx.x - D;
+  return (t >= 0 && t < nvalid) ? to_f32(((const Tin*)a.beta)[(row0 + t) * a.H + h]) : 0.0f;
+}
+
+// Asynchronous 16-byte copy global -> shared (zero-filled when !valid; the
+// source address is then not read).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Rows row0 .. row0 + 15 of head h of a [tokens, H, D] tensor into a dense
+// [16][D] shared tile with cp.async (rows past nvalid zero-filled).
+template <typename T>
+__device__ __forceinline__ void stage_rows(const T* g, T* s, const BwdDev& a, int64_t row0, int h,
+                                           int nvalid) {
+  constexpr int kUnits = (int)(D * sizeof(T) / 16);  // 16-byte pieces per row
+  constexpr int kElems = (int)(16 / sizeof(T));
+  const T* g0 = g + (row0 * a.H + h) * D;
+  for (int u = threadIdx.x; u < C * kUnits; u += kThreads) {
+    const int t = u / kUnits, o = (u % kUnits) * kElems;
+    const bool ok = t < nvalid;
+    cp_async16(s + t * D + o, (ok ? g0 + (int64_t)t * a.H * D : g0) + o, ok);
   }
 }
 
@@ -420,21 +450,37 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_states_kernel(const BwdDe
   float* Tb = M + SM16_F;
   float* ec = Tb + SM16_F;
   float* bt = ec + D;
+  Tin* sth = (Tin*)(bt + C);  // staged theta, k, v of the next chunk: [16][D] each
+  Tin* sk = sth + C * D;
+  Tin* sv = sk + C * D;
   const int tid = threadIdx.x;
   const int64_t chain = blockIdx.x, b = chain / a.H;
   const int h = (int)(chain - b * a.H);
   float* Sw = a.ws_S + (size_t)chain * a.nch * kStateF;
+  auto stage = [&](int n) -> float {  // issue chunk n's copies; returns its beta for this thread
+    const int nv = min(C, a.T - n * C);
+    const int64_t r0 = b * a.T + (int64_t)n * C;
+    stage_rows((const Tin*)a.theta, sth, a, r0, h, nv);
+    stage_rows((const Tin*)a.k, sk, a, r0, h, nv);
+    stage_rows((const Tin*)a.v, sv, a, r0, h, nv);
+    cp_async_commit();
+    return load_beta<Tin>(a, r0, h, nv);
+  };
 
   float st[8][8];
   state_load(st, a.init_state ? a.init_state + chain * kStateF : nullptr);
+  float bnext = a.nch > 1 ? stage(0) : 0.0f;
   for (int n = 0; n < a.nch; ++n) {
     state_store(st, Sw + (size_t)n * kStateF, D);
     if (n + 1 == a.nch) break;  // the last chunk's end state is not needed
     state_store(st, S, LD);
     const int t0 = n * C, nvalid = min(C, a.T - t0);
-    const int64_t row0 = b * a.T + t0;
-    load_chunk<Tin>(a, row0, h, nvalid, nullptr, Kt, 1.0f, Kh, KhC, nullptr, nullptr, ec, bt, V);
+    cp_async_wait_all();
+    __syncthreads();  // the staged chunk is complete, and the previous chunk's reads are done
+    load_chunk<Tin>(sth, sk, nullptr, sv, D, bnext, a.g_min, a.log_decay, nvalid, nullptr, Kt,
+                    1.0f, Kh, KhC, nullptr, nullptr, ec, bt, V);
     __syncthreads();
+    if (n + 2 < a.nch) bnext = stage(n + 1);  // overlaps this chunk's products
     {
       const int m = tid >> 4, nn = tid & 15;
       Ab[m * LS + nn] = nn < m ? dot128(Kt, m, Kh, nn) : 0.0f;
@@ -447,7 +493,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_states_kernel(const BwdDe
     small16<false>(Tb, V, U, 1.0f);  // U = Tb R
     __syncthreads();
     state_update<C>(st, ec, KhC, U);  // S' = Diag(ec) S + KhC^T U
-    __syncthreads();
   }
 }
 
@@ -471,22 +516,41 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_reverse_kernel(const BwdD
   float* TbT = Tb + SM16_F;
   float* ec = TbT + SM16_F;
   float* bt = ec + D;
+  float* sdo = bt + C;  // staged d_out, theta, k, q of the next chunk: [16][D] each
+  Tin* sth = (Tin*)(sdo + C * D);
+  Tin* sk = sth + C * D;
+  Tin* sq = sk + C * D;
   const int tid = threadIdx.x;
   const int64_t chain = blockIdx.x, b = chain / a.H;
   const int h = (int)(chain - b * a.H);
   float* dSw = a.ws_dS + (size_t)chain * a.nch * kStateF;
   float* dUw = a.ws_dU + (size_t)chain * a.nch * C * D;
+  auto stage = [&](int n) -> float {  // issue chunk n's copies; returns its beta for this thread
+    const int nv = min(C, a.T - n * C);
+    const int64_t r0 = b * a.T + (int64_t)n * C;
+    stage_rows(a.d_out, sdo, a, r0, h, nv);
+    stage_rows((const Tin*)a.theta, sth, a, r0, h, nv);
+    stage_rows((const Tin*)a.k, sk, a, r0, h, nv);
+    stage_rows((const Tin*)a.q, sq, a, r0, h, nv);
+    cp_async_commit();
+    return load_beta<Tin>(a, r0, h, nv);
+  };
 
   float st[8][8];
   state_load(st, a.d_final ? a.d_final + chain * kStateF : nullptr);
+  float bnext = stage(a.nch - 1);
   for (int n = a.nch - 1; n >= 0; --n) {
     state_store(st, dSw + (size_t)n * kStateF, D);
     state_store(st, dS, LD);
     const int t0 = n * C, nvalid = min(C, a.T - t0);
     const int64_t row0 = b * a.T + t0;
-    load_chunk<Tin>(a, row0, h, nvalid, Qt, mKt, -1.0f, Kh, KhC, nullptr, nullptr, ec, bt, nullptr);
-    load_dout(a, row0, h, nvalid, dO);
+    cp_async_wait_all();
+    __syncthreads();  // the staged chunk is complete, and the previous chunk's reads are done
+    load_chunk<Tin>(sth, sk, sq, nullptr, D, bnext, a.g_min, a.log_decay, nvalid, Qt, mKt, -1.0f,
+                    Kh, KhC, nullptr, nullptr, ec, bt, nullptr);
+    for (int e = tid; e < C * D; e += kThreads) dO[(e >> 7) * LD + (e & (D - 1))] = sdo[e];
     __syncthreads();
+    if (n > 0) bnext = stage(n - 1);  // overlaps this chunk's products
     {
       const int m = tid >> 4, nn = tid & 15;
       Ab[m * LS + nn] = nn < m ? -dot128(mKt, m, Kh, nn) : 0.0f;
@@ -510,7 +574,6 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_reverse_kernel(const BwdD
       if (t < nvalid) a.dv[((row0 + t) * a.H + h) * D + c] = dR[t * LD + c];
     }
     state_update<2 * C>(st, ec, Qt, dO);  // dS = Diag(ec) dS' + [Qt; -Kt]^T [dO; dR]
-    __syncthreads();
   }
   if (a.d_init) state_store(st, a.d_init + chain * kStateF, D);
 }
@@ -561,7 +624,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
   const float* dUg = a.ws_dU + cidx * C * D;
 
   // ---- operands of the chunk, S, dO and dU
-  load_chunk<Tin>(a, row0, h, nvalid, Qt, Kt, 1.0f, Kh, KhC, EGt, dgt, ec, bt, V);
+  {
+    const int64_t g0 = (row0 * a.H + h) * D;
+    load_chunk<Tin>((const Tin*)a.theta + g0, (const Tin*)a.k + g0, (const Tin*)a.q + g0,
+                    (const Tin*)a.v + g0, (int64_t)a.H * D, load_beta<Tin>(a, row0, h, nvalid),
+                    a.g_min, a.log_decay, nvalid, Qt, Kt, 1.0f, Kh, KhC, EGt, dgt, ec, bt, V);
+  }
   load_dout(a, row0, h, nvalid, X);
   {
     float4 u[2], x[16];
@@ -586,6 +654,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
       *(float4*)(S + (e >> 5) * LD + (e & 31) * 4) = x[i];
     }
   }
+  // this thread's tile of dS', loaded now so that its latency overlaps the
+  // products that need only S
+  float d[8][8];
+  state_load(d, dSg);
   __syncthreads();
   {
     const int m = tid >> 4, nn = tid & 15;
@@ -629,10 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
     }
   }
   reduce_parts<2 * C, 2>(part, X, nullptr, 1.0f);  // [dQt; dKt], the S^T parts
-  float d[8][8];
   {
     // dec_i = sum_j dS'_ij S_ij: row partials of this thread's tile
-    state_load(d, dSg);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       float s = 0.0f;
@@ -732,23 +802,31 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
   }
 }
 
-constexpr size_t kSmemStates = (size_t)(STATE_F + 9 * TILE_F + 3 * SM16_F + D + C) * 4;
-constexpr size_t kSmemReverse = (size_t)(STATE_F + 11 * TILE_F + 5 * SM16_F + D + C) * 4;
+template <typename Tin>
+constexpr size_t smem_states() {
+  return (size_t)(STATE_F + 9 * TILE_F + 3 * SM16_F + D + C) * 4 + 3 * C * D * sizeof(Tin);
+}
+template <typename Tin>
+constexpr size_t smem_reverse() {
+  return (size_t)(STATE_F + 11 * TILE_F + 5 * SM16_F + D + C + C * D) * 4 + 3 * C * D * sizeof(Tin);
+}
 constexpr size_t kSmemGrads = (size_t)(STATE_F + 16 * TILE_F + 11 * SM16_F + 2 * D + 3 * C) * 4;
-static_assert(kSmemGrads <= 232448 && kSmemReverse <= 232448, "shared memory budget");
+static_assert(kSmemGrads <= 232448 && smem_reverse<float>() <= 232448 &&
+                  smem_states<float>() <= 232448,
+              "shared memory budget");
 
 template <typename Tin>
 int launch_bwd_t(const BwdDev& d, int64_t chains, cudaStream_t stream) {
   const void* fns[3] = {(const void*)kda_bwd_states_kernel<Tin>,
                         (const void*)kda_bwd_reverse_kernel<Tin>,
                         (const void*)kda_bwd_grads_kernel<Tin>};
-  const size_t smem[3] = {kSmemStates, kSmemReverse, kSmemGrads};
+  const size_t smem[3] = {smem_states<Tin>(), smem_reverse<Tin>(), kSmemGrads};
   for (int i = 0; i < 3; ++i)
     if (cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem[i]) !=
         cudaSuccess)
       return KDA_ERR_LAUNCH;
-  kda_bwd_states_kernel<Tin><<<(unsigned)chains, kThreads, kSmemStates, stream>>>(d);
-  kda_bwd_reverse_kernel<Tin><<<(unsigned)chains, kThreads, kSmemReverse, stream>>>(d);
+  kda_bwd_states_kernel<Tin><<<(unsigned)chains, kThreads, smem[0], stream>>>(d);
+  kda_bwd_reverse_kernel<Tin><<<(unsigned)chains, kThreads, smem[1], stream>>>(d);
   kda_bwd_grads_kernel<Tin><<<(unsigned)(chains * d.nch), kThreads, kSmemGrads, stream>>>(d);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
