@@ -184,9 +184,10 @@ KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* args, int segments, void
  * respect to q, k, v, theta, beta and the initial state (the reverse pass of
  * the recurrence of "Kimi K3 Deep Dive", section "Core Innovation 1"), in fp32
  * on CUDA cores, in chunked (WY) form: a forward pass that stores the state at
- * every 16-token chunk start, a reverse pass that carries the state gradient
- * and stores it at every chunk end, and one parallel pass over all chunks for
- * the remaining gradients (three kernel launches on `stream`).
+ * every 16-token chunk start and a reverse pass that carries the state
+ * gradient and stores it at every chunk end (one kernel launch, run side by
+ * side), then one parallel pass over all chunks for the remaining gradients
+ * (a second launch on `stream`).
  * Requires dk = dv = 128 and a fixed-length batch.  Layouts as kda_chunk_fwd:
  * q, k, theta, dq, dk, dtheta [B,T,H,dk]; v, d_out, dv [B,T,H,dv]; beta,
  * dbeta [B,T,H]; init_state, d_final, d_init [B,H,dk,dv] fp32 (each of the

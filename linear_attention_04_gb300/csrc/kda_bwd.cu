@@ -24,16 +24,18 @@
 //   (summed as sum_{s >= t} (dG_s + dKhC_s KhC_s) + sum_{s < t} dKhC_s KhC_s + dec ec),
 //   dtheta = dg g_min sigmoid(theta) sigmoid(-theta)   (dg for a given log-decay).
 //
-// Three launches over a caller workspace:
-//   1. kda_bwd_states_kernel  (one CTA per chain): the forward recurrence,
-//      writing the state at the start of every chunk;
-//   2. kda_bwd_reverse_kernel (one CTA per chain): the reverse recurrence of
-//      dS, writing dS' and dU of every chunk, and dV;
-//   3. kda_bwd_grads_kernel   (one CTA per chunk, all chunks in parallel):
-//      every other gradient from S, dS', dU and the chunk's inputs.
-// Launches 1 and 2 carry their 128 x 128 state in registers (an 8 x 8 tile
-// per thread) with a copy in shared memory for the products that contract
-// over it.  Every product is an fp32 FMA over shared-memory operands.
+// Two launches over a caller workspace:
+//   1. kda_bwd_recurrences_kernel, two CTAs per chain (independent of each
+//      other): the forward recurrence, writing the state at the start of every
+//      chunk; and the reverse recurrence of dS, writing dS' and dU of every
+//      chunk, and dV;
+//   2. kda_bwd_grads_kernel, one CTA per chunk, all chunks in parallel: every
+//      other gradient from S, dS', dU and the chunk's inputs.
+// The recurrences carry their 128 x 128 state in registers (an 8 x 8 tile per
+// thread) with a copy in shared memory for the products that contract over
+// it, and stage the next chunk's inputs in shared memory with cp.async while
+// the current chunk computes.  Every product is an fp32 FMA over shared-memory
+// operands.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -304,7 +306,7 @@ __device__ __forceinline__ void load_chunk(const Tin* th0, const Tin* k0, const 
       KhC[t * LD + c] = kr[t] * P;
       P *= egr[t];
     }
-  } else {
+  } else if (tid < 2 * D) {
     const int c = tid - D;
     if (V) {
       float vr[C];
@@ -434,9 +436,9 @@ __device__ __forceinline__ void state_update(float (&st)[8][8], const float* ec,
   gemm_acc<8, 8, false, true>(st, A, LD, 8 * ig, B, LD, 4 * jg, 64, 0, K);
 }
 
-// ------------------------------------------------------------------ launch 1
+// ------------------------------------------------------- forward recurrence
 template <typename Tin>
-__global__ void __launch_bounds__(kThreads, 1) kda_bwd_states_kernel(const BwdDev a) {
+__device__ __forceinline__ void states_chain(const BwdDev& a, int64_t chain) {
   extern __shared__ __align__(16) float smf[];
   float* S = smf;
   float* Kt = S + STATE_F;
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_states_kernel(const BwdDe
   Tin* sk = sth + C * D;
   Tin* sv = sk + C * D;
   const int tid = threadIdx.x;
-  const int64_t chain = blockIdx.x, b = chain / a.H;
+  const int64_t b = chain / a.H;
   const int h = (int)(chain - b * a.H);
   float* Sw = a.ws_S + (size_t)chain * a.nch * kStateF;
   auto stage = [&](int n) -> float {  // issue chunk n's copies; returns its beta for this thread
@@ -496,9 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_states_kernel(const BwdDe
   }
 }
 
-// ------------------------------------------------------------------ launch 2
+// ------------------------------------------------------- reverse recurrence
 template <typename Tin>
-__global__ void __launch_bounds__(kThreads, 1) kda_bwd_reverse_kernel(const BwdDev a) {
+__device__ __forceinline__ void reverse_chain(const BwdDev& a, int64_t chain) {
   extern __shared__ __align__(16) float smf[];
   float* dS = smf;
   float* Qt = dS + STATE_F;  // [Qt; -Kt]: 32 rows
@@ -521,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_reverse_kernel(const BwdD
   Tin* sk = sth + C * D;
   Tin* sq = sk + C * D;
   const int tid = threadIdx.x;
-  const int64_t chain = blockIdx.x, b = chain / a.H;
+  const int64_t b = chain / a.H;
   const int h = (int)(chain - b * a.H);
   float* dSw = a.ws_dS + (size_t)chain * a.nch * kStateF;
   float* dUw = a.ws_dU + (size_t)chain * a.nch * C * D;
@@ -578,7 +580,21 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_reverse_kernel(const BwdD
   if (a.d_init) state_store(st, a.d_init + chain * kStateF, D);
 }
 
-// ------------------------------------------------------------------ launch 3
+// The two recurrences are independent of each other and run as one grid: CTAs
+// 0 .. chains-1 run the reverse recurrence (the longer one per chunk) and CTAs
+// chains .. 2 chains-1 the forward one, so that the two sets of chains share
+// the SMs without a wave boundary between them.
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads, 1) kda_bwd_recurrences_kernel(const BwdDev a,
+                                                                          int64_t chains) {
+  const int64_t blk = blockIdx.x;
+  if (blk < chains)
+    reverse_chain<Tin>(a, blk);
+  else
+    states_chain<Tin>(a, blk - chains);
+}
+
+// ------------------------------------------------------ per-chunk gradients
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev a) {
   extern __shared__ __align__(16) float smf[];
@@ -817,16 +833,17 @@ static_assert(kSmemGrads <= 232448 && smem_reverse<float>() <= 232448 &&
 
 template <typename Tin>
 int launch_bwd_t(const BwdDev& d, int64_t chains, cudaStream_t stream) {
-  const void* fns[3] = {(const void*)kda_bwd_states_kernel<Tin>,
-                        (const void*)kda_bwd_reverse_kernel<Tin>,
+  constexpr size_t kSmemRec =
+      smem_states<Tin>() > smem_reverse<Tin>() ? smem_states<Tin>() : smem_reverse<Tin>();
+  const void* fns[2] = {(const void*)kda_bwd_recurrences_kernel<Tin>,
                         (const void*)kda_bwd_grads_kernel<Tin>};
-  const size_t smem[3] = {smem_states<Tin>(), smem_reverse<Tin>(), kSmemGrads};
-  for (int i = 0; i < 3; ++i)
+  const size_t smem[2] = {kSmemRec, kSmemGrads};
+  for (int i = 0; i < 2; ++i)
     if (cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem[i]) !=
         cudaSuccess)
       return KDA_ERR_LAUNCH;
-  kda_bwd_states_kernel<Tin><<<(unsigned)chains, kThreads, smem[0], stream>>>(d);
-  kda_bwd_reverse_kernel<Tin><<<(unsigned)chains, kThreads, smem[1], stream>>>(d);
+  if (2 * chains > (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
+  kda_bwd_recurrences_kernel<Tin><<<(unsigned)(2 * chains), kThreads, kSmemRec, stream>>>(d, chains);
   kda_bwd_grads_kernel<Tin><<<(unsigned)(chains * d.nch), kThreads, kSmemGrads, stream>>>(d);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
