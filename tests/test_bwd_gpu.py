@@ -79,3 +79,21 @@ def test_bwd_fast_decay_multi_chain():
     for name, key in (("dq", "dq"), ("dk", "dk"), ("dv", "dv"), ("dtheta", "dtheta"),
                       ("dbeta", "dbeta"), ("d_init", "dS0")):
         assert_close(f64(got[name]), ref[key], TOL_BWD, f"{name} fast decay")
+
+
+def test_bwd_long_sequence():
+    """T = 1000 (62 whole chunks and a ragged 8-token tail), two heads, an
+    initial state and a final-state gradient: the two recurrences over many
+    chunks and the staged next-chunk inputs at every step."""
+    inp, d_out, d_fin = _case(torch.bfloat16, 1000, H=2, seed=21, init=0.02)
+    ref = backward.bwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["theta"]),
+                       f64(inp["beta"]), -5.0, f64(inp["init_state"]), d_out.double().numpy(),
+                       d_fin.double().numpy())
+    c = lambda x: x.cuda()
+    got = kda_chunk_bwd(c(inp["q"]), c(inp["k"]), c(inp["v"]), c(inp["theta"]), c(inp["beta"]),
+                        c(d_out), -5.0, c(inp["init_state"]), c(d_fin))
+    torch.cuda.synchronize()
+    assert kda_device_status(clear=True) == 0
+    for name, key in (("dq", "dq"), ("dk", "dk"), ("dv", "dv"), ("dtheta", "dtheta"),
+                      ("dbeta", "dbeta"), ("d_init", "dS0")):
+        assert_close(f64(got[name]), ref[key], TOL_BWD, f"{name} T=1000")
