@@ -599,9 +599,10 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 def bwd_flops(w, inp, C=16) -> int:
     """Algorithmic FLOPs of one chunked backward pass: per token-head
     2 (9 d^2 + d^2 / C + 16 C d + 2 C^2) at d = dk = dv -- the chunk products of
-    the three launches (states: Kt S, KhC^T U and the 16 x 16 products; reverse:
-    KhC dS', [Qt; -Kt]^T [dO; dR] and the 16 x 16 products; gradients: Kt S,
-    [dO; -dR] S^T, U dS'^T, dS' * S and the 16 x 16 products)."""
+    the forward recurrence (Kt S, KhC^T U and the 16 x 16 products), the reverse
+    recurrence (KhC dS', [Qt; -Kt]^T [dO; dR] and the 16 x 16 products) and the
+    per-chunk gradient kernel (Kt S, [dO; -dR] S^T, U dS'^T, dS' * S and the
+    16 x 16 products)."""
     d = w.dk
     n = n_tokens(inp) * w.H
     return n * 2 * (9 * d * d + d * d // C + 16 * C * d + 2 * C * C)
