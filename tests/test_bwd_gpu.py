@@ -97,3 +97,33 @@ def test_bwd_long_sequence():
     for name, key in (("dq", "dq"), ("dk", "dk"), ("dv", "dv"), ("dtheta", "dtheta"),
                       ("dbeta", "dbeta"), ("d_init", "dS0")):
         assert_close(f64(got[name]), ref[key], TOL_BWD, f"{name} T=1000")
+
+
+@pytest.mark.parametrize("with_final", [True, False])
+def test_bwd_empty_and_single_token(with_final):
+    """T = 0: no tokens, so the initial state's gradient is the final state's
+    (zero without one) and nothing else is written.  T = 1: one ragged chunk
+    of a single token against the oracle."""
+    B, H = 2, 3
+    g = torch.Generator().manual_seed(31)
+    d_fin = torch.randn(B, H, 128, 128, generator=g) if with_final else None
+    z = lambda *s: torch.zeros(*s, dtype=torch.bfloat16, device="cuda")
+    got = kda_chunk_bwd(z(B, 0, H, 128), z(B, 0, H, 128), z(B, 0, H, 128), z(B, 0, H, 128),
+                        z(B, 0, H), torch.zeros(B, 0, H, 128, device="cuda"), -5.0,
+                        None, d_fin.cuda() if with_final else None)
+    torch.cuda.synchronize()
+    want = d_fin if with_final else torch.zeros(B, H, 128, 128)
+    assert torch.equal(got["d_init"].cpu(), want)
+
+    inp, d_out, d_fin1 = _case(torch.bfloat16, 1, H=H, B=B, seed=32)
+    ref = backward.bwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["theta"]),
+                       f64(inp["beta"]), -5.0, f64(inp["init_state"]), d_out.double().numpy(),
+                       d_fin1.double().numpy() if with_final else None)
+    c = lambda x: None if x is None else x.cuda()
+    got = kda_chunk_bwd(c(inp["q"]), c(inp["k"]), c(inp["v"]), c(inp["theta"]), c(inp["beta"]),
+                        c(d_out), -5.0, c(inp["init_state"]), c(d_fin1) if with_final else None)
+    torch.cuda.synchronize()
+    assert kda_device_status(clear=True) == 0
+    for name, key in (("dq", "dq"), ("dk", "dk"), ("dv", "dv"), ("dtheta", "dtheta"),
+                      ("dbeta", "dbeta"), ("d_init", "dS0")):
+        assert_close(f64(got[name]), ref[key], TOL_BWD, f"{name} T=1")
