@@ -276,13 +276,15 @@ def cpu_baseline(w: Workload, target_s: float, seed: int) -> dict:
 # ----------------------------------------------------------------------------- our arm
 
 def selected_workload(args):
-    """The named workload, with B replaced when --batch is given (smaller
-    profiling cases of the same shape per sequence)."""
+    """The named workload, with B and H replaced when --batch / --heads are
+    given (profiling cases of the same shape per sequence)."""
     w = WORKLOADS[args.workload]
-    if args.batch:
+    if args.batch or args.heads:
         if w.varlen:
-            raise SystemExit("--batch applies to fixed-length workloads only")
-        w = dataclasses.replace(w, B=args.batch)
+            raise SystemExit("--batch and --heads apply to fixed-length workloads only")
+        B, H = args.batch or w.B, args.heads or w.H
+        # a new name: captures recorded for the named workload do not apply
+        w = dataclasses.replace(w, B=B, H=H, name=f"{w.name}-B{B}-H{H}")
     return w
 
 
@@ -687,6 +689,8 @@ def main(argv=None):
     ap.add_argument("--path", choices=["auto", "simt", "tc", "mma"], default="auto")
     ap.add_argument("--batch", type=int, default=0,
                     help="replace the workload's B (fixed-length workloads; profiling cases)")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="replace the workload's H (fixed-length workloads; profiling cases)")
     ap.add_argument("--seed", type=int, default=20261204)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
