@@ -55,13 +55,15 @@ def n_tokens(inp: dict) -> int:
     return int(sum(inp["lengths"]))
 
 
-def algorithmic_bytes(w: Workload, inp: dict, out_bytes: int = 4) -> int:
+def algorithmic_bytes(w: Workload, inp: dict, out_bytes: int | None = None) -> int:
     """Minimum HBM bytes of one pass: q, k, theta, v, beta read and out written
-    (e*(3dk+dv) + e + e_out*dv per token-head; out is fp32 by default), plus
-    the fp32 final state written and the fp32 initial state read when given
-    (4*dk*dv per chain each)."""
+    (e*(3dk+dv) + e + e_out*dv per token-head), plus the fp32 final state
+    written and the fp32 initial state read when given (4*dk*dv per chain
+    each).  e_out defaults to the input element size e (the counting rule of
+    the scope table: 1282 B per token-head for bf16 at d = 128); pass 4 for
+    the bytes of the fp32 output the library writes by default (1538 B)."""
     e = torch.tensor([], dtype=w.dtype).element_size()
-    per = e * (3 * w.dk + w.dv) + e + out_bytes * w.dv
+    per = e * (3 * w.dk + w.dv) + e + (e if out_bytes is None else out_bytes) * w.dv
     chains = inp["N"] * w.H
     state = 4 * w.dk * w.dv * chains
     return token_heads(w, inp) * per + state * (2 if inp["init_state"] is not None else 1)
@@ -87,8 +89,8 @@ def measured_peaks() -> tuple[dict, str]:
 KERNEL_SOURCES = {
     "kda_fwd_mma_kernel": ["csrc/kda_mma.cu", "csrc/kda_tmap.cu", "csrc/kda_sm100.cuh",
                            "csrc/kda_device.cuh", "csrc/kda_internal.cuh"],
-    "kda_fwd_tc_kernel": ["csrc/kda_tc.cu", "csrc/kda_tmap.cu", "csrc/kda_sm100.cuh",
-                          "csrc/kda_device.cuh", "csrc/kda_internal.cuh"],
+    "kda_fwd_tc32_kernel": ["csrc/kda_tc32.cu", "csrc/kda_tmap.cu", "csrc/kda_sm100.cuh",
+                            "csrc/kda_device.cuh", "csrc/kda_internal.cuh"],
     "kda_decode_kernel": ["csrc/kda_decode.cu", "csrc/kda_device.cuh", "csrc/kda_internal.cuh"],
     "kda_bwd": ["csrc/kda_bwd.cu", "csrc/kda_device.cuh", "csrc/kda_internal.cuh"],
 }
@@ -307,12 +309,14 @@ def run_ours(args, rank, world, local):
         from linear_attention_04_gb300 import kda_chunk_fwd_segmented, kda_segmented_workspace_size
         ws = torch.empty(kda_segmented_workspace_size(w.B, w.H, w.T, w.dk, w.dv, args.segments),
                          dtype=torch.uint8, device=dev)
-        path = f"segmented x{args.segments} (mma)"
+        seg_kernel = "mma" if path == "mma" else path
+        path = f"segmented x{args.segments} ({seg_kernel})"
 
     def step():
         if ws is not None:
             kda_chunk_fwd_segmented(q, k, v, th, be, w.g_min, init, out, fin,
-                                    segments=args.segments, workspace=ws, stream=stream)
+                                    segments=args.segments, workspace=ws, path=seg_kernel,
+                                    stream=stream)
         else:
             kda_chunk_fwd(q, k, v, th, be, w.g_min, init, out, fin, cu, path=path, stream=stream)
 
@@ -360,17 +364,28 @@ def run_ours(args, rank, world, local):
     ms_per_step = total_ms / args.steps
     avg_launch_s = statistics.mean(launch_ms) / 1e3
     peaks, peak_src = measured_peaks()
-    alg = algorithmic_bytes(w, inp)
+    alg = algorithmic_bytes(w, inp)                  # out counted at the input's element size
+    alg32 = algorithmic_bytes(w, inp, out_bytes=4)   # out counted as the fp32 the kernel writes
     flops = chunk_gemm_flops(w, inp)
     achieved = alg / avg_launch_s / 1e9
-    kname = {"tc": "kda_fwd_tc_kernel", "mma": "kda_fwd_mma_kernel"}.get(path, "kda_fwd_simt_kernel")
+    achieved32 = alg32 / avg_launch_s / 1e9
+    kernels = {"tc": "kda_fwd_tc32_kernel", "tc_split": "kda_fwd_tc32_kernel",
+               "mma": "kda_fwd_mma_kernel"}
+    kname = kernels.get(path, "kda_fwd_simt_kernel")
     if ws is not None:
-        kname = "kda_fwd_mma_kernel"
+        kname = kernels.get(seg_kernel, "kda_fwd_tc32_kernel")
     traffic, traffic_src = traffic_from_profiles(kname, w.name)
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "traffic": traffic, "peak_source": f"hbm_gbs of {peak_src}",
             "kernel": kname, "algorithmic_bytes_per_launch": alg,
+            "bytes_counted": "q, k, theta, v, beta read and out written at the input element "
+                             "size (2 B for bf16) plus the fp32 final state",
+            "fp32_out": {"achieved": round(achieved32, 1),
+                         "frac": round(achieved32 / peaks["hbm_gbs"], 4),
+                         "algorithmic_bytes_per_launch": alg32,
+                         "bytes_counted": "as above with out at 4 B (the fp32 output the "
+                                          "kernel writes)"},
             "tensor": {"achieved_tflops": round(flops / avg_launch_s / 1e12, 2),
                        "peak_tflops": peaks["bf16_tflops"],
                        "frac": round(flops / avg_launch_s / 1e12 / peaks["bf16_tflops"], 4),
@@ -421,7 +436,7 @@ def run_ours(args, rank, world, local):
             if ws is not None:
                 kda_chunk_fwd_segmented(dq, dk_, dv_, dth, dbe, w.g_min, b["init"], b["out"],
                                         b["fin"], segments=args.segments, workspace=ws,
-                                        stream=stream)
+                                        path=seg_kernel, stream=stream)
             else:
                 kda_chunk_fwd(dq, dk_, dv_, dth, dbe, w.g_min, b["init"], b["out"], b["fin"], cu,
                               path=path, stream=stream)
@@ -470,7 +485,7 @@ def run_ours(args, rank, world, local):
                        "global_batch": w.B * world, "parallelism": f"sequence-shard x{world}",
                        "path": path, "seed": args.seed,
                        "l2": "inputs larger than L2 (no flush): "
-                             f"{alg / 1e9:.2f} GB per step vs 126 MB L2"},
+                             f"{alg32 / 1e9:.2f} GB per step vs 126 MB L2"},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
             "clocks": clocks.summary(t_wall0, t_wall1),
             "kernel_ms": {"mean": round(statistics.mean(launch_ms), 4),
@@ -686,7 +701,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="train_bf16")
-    ap.add_argument("--path", choices=["auto", "simt", "tc", "mma"], default="auto")
+    ap.add_argument("--path", choices=["auto", "simt", "tc", "tc_split", "mma"], default="auto")
     ap.add_argument("--batch", type=int, default=0,
                     help="replace the workload's B (fixed-length workloads; profiling cases)")
     ap.add_argument("--heads", type=int, default=0,

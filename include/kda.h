@@ -15,7 +15,10 @@
  * "Kimi K3" explainer (section "Across the sequence") describes: a fixed-size
  * state S in R^{dk x dv} that each token reads, selectively forgets and writes.
  * The library evaluates it chunk by chunk (16-token chunks, "Kimi K3 Deep
- * Dive", section "The Problem"), every tile through dense products.
+ * Dive", section "The Problem"), every tile through dense products; the
+ * tcgen05 path (KDA_PATH_TC) pairs two chunks into one 32-token state step
+ * whose decay factors are anchored at the boundary between the two chunks,
+ * so every factor stays within e^{+-80} as in a single 16-token chunk.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -38,6 +41,11 @@
  *   final_state == NULL: the final state is not written.
  *   Lengths need not be multiples of 16: the last chunk of a sequence is
  *   masked (exactly as if padded with k = v = beta = 0, theta = -inf).
+ *   The kernels check the packing table on the device, each block for the
+ *   sequence it runs (cu_seqlens[0] = 0, cu_seqlens[B] = T, 0 <= start <= end
+ *   <= T): a block whose check fails stores nothing and records
+ *   KDA_ERR_BAD_SEQLENS in the status word (kda_device_status); no store ever
+ *   leaves the rows [0, T) of the tensors.
  *
  * Semantics: no scaling of q and no normalisation of q or k is applied (the
  * caller normalises); beta is used as given (already in (0, 1)); g_min must be
@@ -79,12 +87,14 @@ extern "C" {
 #define KDA_ERR_CUDA (-6)               /* another CUDA runtime error                    */
 #define KDA_ERR_UNSUPPORTED_SHAPE (-7)  /* dk/dv outside {16,32,64,128} for this path    */
 #define KDA_ERR_SCRATCH_TOO_SMALL (-8)  /* the fixed scratch area cannot hold the call   */
+#define KDA_ERR_BAD_SEQLENS (-9)        /* device status: cu_seqlens not a valid packing  */
 
 /* kernel path selection for kda_chunk_fwd_ex */
-#define KDA_PATH_AUTO 0 /* KDA_PATH_MMA for bf16 with dk = dv = 128, else SIMT        */
-#define KDA_PATH_SIMT 1 /* fp32 CUDA-core path (any supported dtype/shape)             */
-#define KDA_PATH_TC 2   /* tcgen05/TMEM tensor-core path (bf16, dk = dv = 128)         */
-#define KDA_PATH_MMA 3  /* register-resident mma.sync path (bf16, dk = dv = 128)       */
+#define KDA_PATH_AUTO 0     /* KDA_PATH_MMA for bf16 with dk = dv = 128, else SIMT          */
+#define KDA_PATH_SIMT 1     /* fp32 CUDA-core path (any supported dtype/shape)              */
+#define KDA_PATH_TC 2       /* tcgen05/TMEM path, state stepped per 32 tokens (bf16, 128)   */
+#define KDA_PATH_MMA 3      /* register-resident mma.sync path, 16-token steps (bf16, 128)  */
+#define KDA_PATH_TC_SPLIT 4 /* KDA_PATH_TC with the state's bf16 copy as a high/low pair    */
 
 /* gate parameterisation (kda_fwd_args.gate) */
 #define KDA_GATE_SIGMOID 0   /* g = g_min * sigmoid(theta): the bounded gate (default)     */
@@ -97,7 +107,12 @@ extern "C" {
 /*
  * kda_chunk_fwd -- bf16 q, k, v, theta and beta; fp32 out; fp32 states.
  * fp32 arithmetic in the gate, the cumulative sums and the state; bf16
- * tensor-core operands with fp32 accumulation in the chunk products.
+ * tensor-core operands with fp32 accumulation in the chunk products (the
+ * register-resident path, KDA_PATH_MMA).  kda_chunk_fwd_ex selects the
+ * tcgen05 path (KDA_PATH_TC), whose products use tf32 operands for the
+ * decayed Gram tile and bf16 high/low pairs for the chunk-local factors
+ * (U, P, and the decayed keys of the last state update): more accurate when
+ * the decay is slow, at a higher cost per token.
  * `out` is fp32 because the outputs of this operator are heavy-tailed (the
  * largest |o| is typically 14-18 times the RMS of o), so rounding even an
  * exact result to bf16 already moves the largest entries by about 4e-2 of
@@ -125,16 +140,20 @@ KDA_API int kda_chunk_fwd_f32(const float* q, const float* k, const float* v, co
  * path chosen explicitly.  `dtype` (KDA_DTYPE_*) is the type of q, k, v,
  * theta and beta; `out_dtype` that of out (KDA_DTYPE_F32, or KDA_DTYPE_BF16
  * to halve the output bytes at the cost of bf16 rounding of o; fp32 inputs
- * require an fp32 out).  `path` is KDA_PATH_*; KDA_PATH_TC and KDA_PATH_MMA
- * require bf16 inputs and dk = dv = 128 (else KDA_ERR_UNSUPPORTED_SHAPE).
+ * require an fp32 out).  `path` is KDA_PATH_*; KDA_PATH_TC, KDA_PATH_TC_SPLIT
+ * and KDA_PATH_MMA require bf16 inputs and dk = dv = 128 (else
+ * KDA_ERR_UNSUPPORTED_SHAPE).  KDA_PATH_TC_SPLIT is KDA_PATH_TC with the
+ * state's bf16 copy kept as a high/low pair in the state read-out products:
+ * more accurate when many channels decay slowly (the state then carries
+ * many chunks), at the cost of a second read-out product per 32 tokens.
  * `gate` selects how theta becomes the log-decay.  KDA_GATE_SIGMOID is the
  * bounded gate of the pages, under which every in-chunk factor e^{-G} stays
  * at or below e^{80}.  KDA_GATE_LOG_DECAY takes g from theta as given (any
  * g <= 0, for instance -softplus of a logit) with no bound: the tensor-core
- * paths then need the in-chunk sum of |g| over any 16 tokens to stay below
- * about 88 (fp32 and bf16 overflow of e^{-G}), else their results are not
- * finite; the SIMT path has the same limit.  KDA_PATH_TC supports only
- * KDA_GATE_SIGMOID. */
+ * paths then need the sum of |g| over every 16-token chunk (chunks counted
+ * from the sequence start) to stay below about 88 (fp32 and bf16 overflow of
+ * e^{-G}), else their results are not finite; the SIMT path has the same
+ * limit. */
 typedef struct kda_fwd_args {
   const void* q;
   const void* k;
@@ -161,14 +180,17 @@ KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* args, cudaStream_t stream);
  * very long sequences).  The recurrence is affine in the state, so over any
  * segment S_end = Phi S_start + S_loc, with S_loc the end state from a zero
  * start and Phi (dk x dk) the end state with v = 0 from the identity; each
- * chain is cut into `segments` pieces of whole 16-token chunks, the pieces'
+ * chain is cut into `segments` pieces of whole 32-token units, the pieces'
  * (Phi, S_loc) are computed in parallel, chained in fp32, and every piece is
  * then run from its start state.  Work grows by about (2P - 3) / P for P
- * segments and runs on otherwise idle SMs.  Same arithmetic as the
- * register-resident path (results equal up to rounding order).
+ * segments and runs on otherwise idle SMs.  Results equal the unsegmented
+ * call up to rounding order.
  * Requires bf16 inputs, dk = dv = 128 and a fixed-length batch (cu_seqlens
- * NULL; else KDA_ERR_UNSUPPORTED_SHAPE / KDA_ERR_INVALID_ARG); args->path is
- * ignored.  segments = 1 runs the plain path.
+ * NULL; else KDA_ERR_UNSUPPORTED_SHAPE / KDA_ERR_INVALID_ARG) with B * T
+ * below 2^31.  args->path picks the kernel that runs the pieces:
+ * KDA_PATH_MMA the register-resident one, KDA_PATH_TC_SPLIT the tcgen05 one
+ * with the split state copy, any other value the tcgen05 one.  segments = 1
+ * runs the plain path.
  * `workspace`: device memory of at least kda_segmented_workspace_size(B, H, T,
  * dk, dv, segments) bytes, 256-byte aligned, owned by the caller, contents
  * need not be initialised; it is scratch until the stream has passed this
@@ -229,9 +251,10 @@ KDA_API int kda_chunk_bwd(const kda_bwd_args* args, void* workspace, size_t work
 
 /*
  * kda_selftest_withheld_handoff -- test hook for the failure path (no
- * counterpart on the pages).  Runs the register-resident kernel on the first
- * (sequence, head) chain of `args` (bf16, dk = dv = 128, fixed length,
- * T >= 16) with the producer side withholding the hand-off of the first
+ * counterpart on the pages).  Runs one kernel on the first (sequence, head)
+ * chain of `args` (bf16, dk = dv = 128, fixed length, T >= 16): the
+ * register-resident kernel if args->path is KDA_PATH_MMA, else the tcgen05
+ * kernel, with the producer side withholding the hand-off of the first
  * chunk, and every bounded wait limited to `wait_limit_ns` (> 0).  The
  * consumer's wait runs out, the kernel stops all its roles, and the device
  * status word reads KDA_ERR_DEVICE_TIMEOUT after the stream is synchronised
@@ -242,6 +265,28 @@ KDA_API int kda_chunk_bwd(const kda_bwd_args* args, void* workspace, size_t work
 KDA_API int kda_selftest_withheld_handoff(const kda_fwd_args* args, long long wait_limit_ns,
                                           void* workspace, size_t workspace_bytes,
                                           cudaStream_t stream);
+
+/*
+ * kda_debug_fwd_stages -- test hook (no counterpart on the pages): runs the
+ * tcgen05 path (KDA_PATH_TC, or KDA_PATH_TC_SPLIT if args->path says so) on
+ * `args` exactly as kda_chunk_fwd_ex does, and in addition writes the
+ * intermediate stages of the first (sequence, head) chain -- rank 0 of the
+ * launch -- for its first `nsc` 32-token units into `dump` (device, fp32,
+ * 16-byte aligned, nsc * kda_debug_stage_floats() floats, caller-owned).
+ * Per 32-token unit, in this order (row-major):
+ *   A [32][32]   beta_r * (decayed k_r . k_s) for s < r, else 0
+ *   P [32][32]   decayed q_t . k_s for s < t, else 0
+ *   T [32][32]   (I + A)^{-1} (lower triangular)
+ *   W [32][128]  T Diag(beta) (K e^{G}), G the cumulative log-decay from the
+ *                unit's start
+ *   U [32][128]  T Diag(beta) V - W S (S the state at the unit's start)
+ *   eG [128]     e^{G} at the unit's last token
+ *   qk [32]      q_t . k_t
+ * Requires bf16 inputs and dk = dv = 128.  Returns KDA_OK or KDA_ERR_*.
+ */
+KDA_API int kda_debug_fwd_stages(const kda_fwd_args* args, float* dump, int nsc,
+                                 cudaStream_t stream);
+KDA_API int kda_debug_stage_floats(void);
 
 /* Bytes of the scratch area built into the library for
  * kda_chunk_fwd_segmented_noalloc (24 MiB per device). */
@@ -262,9 +307,12 @@ KDA_API int kda_selftest_withheld_handoff(const kda_fwd_args* args, long long wa
  * - There is one area per device: calls on the same device whose execution
  *   may overlap (other streams, other host threads) race on it and must be
  *   serialised by the caller.
- * - The area's device address is looked up once per device, by the first
- *   call made with that device current; make that first call before any
- *   stream capture on that device.
+ * - The area's device address is looked up by the first call made with that
+ *   device current (a failed lookup is retried by the next call); make that
+ *   first call before any stream capture on that device.  cudaDeviceReset
+ *   discards the area: do not call this entry point on a device after
+ *   resetting it in the same process.
+ * - B * T must stay below 2^31 (KDA_ERR_INVALID_ARG).
  * Arguments, requirements and results otherwise as kda_chunk_fwd_segmented.
  */
 KDA_API int kda_chunk_fwd_segmented_noalloc(const kda_fwd_args* args, int segments,
@@ -291,7 +339,8 @@ KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const v
                             const void* beta, float g_min, float* state, float* out, int N, int H,
                             int dk, int dv, int dtype, cudaStream_t stream);
 
-/* Reads the current device's status word (KDA_OK or KDA_ERR_DEVICE_TIMEOUT).
+/* Reads the current device's status word (KDA_OK, KDA_ERR_DEVICE_TIMEOUT or
+ * KDA_ERR_BAD_SEQLENS).
  * Synchronous with respect to the device's prior work only through the copy:
  * call after synchronising the streams that ran the forward pass.  A nonzero
  * `clear` resets the word to KDA_OK. */

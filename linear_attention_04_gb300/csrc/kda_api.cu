@@ -59,7 +59,7 @@ int validate(const kda_fwd_args* a) {
   if (a->out_dtype != KDA_DTYPE_BF16 && a->out_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
   if (a->dtype == KDA_DTYPE_F32 && a->out_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
   if (a->path != KDA_PATH_AUTO && a->path != KDA_PATH_SIMT && a->path != KDA_PATH_TC &&
-      a->path != KDA_PATH_MMA)
+      a->path != KDA_PATH_MMA && a->path != KDA_PATH_TC_SPLIT)
     return KDA_ERR_INVALID_ARG;
   if (!shape_ok(a->dk) || !shape_ok(a->dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
   // sizes must fit the 32-bit grid and 64-bit offsets used by the kernels
@@ -89,7 +89,7 @@ KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* a, cudaStream_t stream) {
   if (rc != KDA_OK) return rc;
   int path = a->path;
   if (path == KDA_PATH_AUTO) path = kda_select_path(a->dtype, a->dk, a->dv);
-  if (path == KDA_PATH_TC && (!kda::tc_supported(a->dtype, a->dk, a->dv) || a->gate != KDA_GATE_SIGMOID))
+  if ((path == KDA_PATH_TC || path == KDA_PATH_TC_SPLIT) && !kda::tc32_supported(a->dtype, a->dk, a->dv))
     return KDA_ERR_UNSUPPORTED_SHAPE;
   if (path == KDA_PATH_MMA && !kda::mma_supported(a->dtype, a->dk, a->dv))
     return KDA_ERR_UNSUPPORTED_SHAPE;
@@ -127,7 +127,8 @@ KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* a, cudaStream_t stream) {
     }
     return KDA_OK;
   }
-  if (path == KDA_PATH_TC) return kda::launch_tc(p, stream);
+  if (path == KDA_PATH_TC || path == KDA_PATH_TC_SPLIT)
+    return kda::launch_tc32_jobs(p, nullptr, 0, stream, 0, path == KDA_PATH_TC_SPLIT);
   if (path == KDA_PATH_MMA) return kda::launch_mma(p, stream);
   return kda::launch_simt(p, stream);
 }
@@ -165,9 +166,12 @@ KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* a, int segments, void* w
   if (segments > 1 && a->T > 0 &&
       (!workspace || workspace_bytes < kda::segmented_workspace_size(a->B, a->H, a->T, segments)))
     return KDA_ERR_INVALID_ARG;
+  if ((int64_t)a->B * a->T > (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
+  // the kernel: the register-resident one for KDA_PATH_MMA, else tcgen05
+  const int kernel = (a->path == KDA_PATH_MMA || a->path == KDA_PATH_TC_SPLIT) ? a->path : KDA_PATH_TC;
   if (a->T == 0) {
     kda_fwd_args b = *a;
-    b.path = KDA_PATH_MMA;
+    b.path = kernel;
     return kda_chunk_fwd_ex(&b, stream);
   }
   rc = kda::check_device();
@@ -191,7 +195,7 @@ KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* a, int segments, void* w
   p.dtype = a->dtype;
   p.out_dtype = a->out_dtype;
   p.gate = a->gate;
-  return kda::launch_segmented(p, segments, workspace, workspace_bytes, stream);
+  return kda::launch_segmented(p, segments, workspace, workspace_bytes, stream, kernel);
 }
 
 KDA_API int kda_chunk_fwd_segmented_noalloc(const kda_fwd_args* a, int segments,
@@ -200,6 +204,7 @@ KDA_API int kda_chunk_fwd_segmented_noalloc(const kda_fwd_args* a, int segments,
   if (rc != KDA_OK) return rc;
   if (a->dtype != KDA_DTYPE_BF16 || a->dk != 128 || a->dv != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
   if (a->cu_seqlens || segments < 1) return KDA_ERR_INVALID_ARG;
+  if ((int64_t)a->B * a->T > (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
   const size_t need = a->T > 0 ? kda::segmented_workspace_size(a->B, a->H, a->T, segments) : 0;
   if (need > kda::kNoallocScratchBytes) return KDA_ERR_SCRATCH_TOO_SMALL;
   rc = kda::check_device();
@@ -312,9 +317,42 @@ KDA_API int kda_selftest_withheld_handoff(const kda_fwd_args* a, long long wait_
   p.out_dtype = a->out_dtype;
   p.gate = a->gate;
   // the job table lives in device memory the copy above fills, in stream order
-  rc = kda::launch_mma_jobs(p, (const kda::SegJob*)workspace, 1, stream, (uint64_t)wait_limit_ns);
-  return rc;
+  const kda::SegJob* jobs = (const kda::SegJob*)workspace;
+  if (a->path == KDA_PATH_MMA) return kda::launch_mma_jobs(p, jobs, 1, stream, (uint64_t)wait_limit_ns);
+  return kda::launch_tc32_jobs(p, jobs, 1, stream, (uint64_t)wait_limit_ns, a->path == KDA_PATH_TC_SPLIT);
 }
+
+KDA_API int kda_debug_fwd_stages(const kda_fwd_args* a, float* dump, int nsc, cudaStream_t stream) {
+  int rc = kda::validate(a);
+  if (rc != KDA_OK) return rc;
+  if (a->dtype != KDA_DTYPE_BF16 || a->dk != 128 || a->dv != 128) return KDA_ERR_UNSUPPORTED_SHAPE;
+  if (a->T <= 0 || nsc < 1 || !dump) return KDA_ERR_INVALID_ARG;
+  if (!kda::aligned16(dump)) return KDA_ERR_MISALIGNED;
+  rc = kda::check_device();
+  if (rc != KDA_OK) return rc;
+  kda::FwdParams p;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.theta = a->theta;
+  p.beta = a->beta;
+  p.g_min = a->g_min;
+  p.init_state = a->init_state;
+  p.out = a->out;
+  p.final_state = a->final_state;
+  p.cu_seqlens = a->cu_seqlens;
+  p.N = a->B;
+  p.H = a->H;
+  p.T = a->T;
+  p.dk = a->dk;
+  p.dv = a->dv;
+  p.dtype = a->dtype;
+  p.out_dtype = a->out_dtype;
+  p.gate = a->gate;
+  return kda::launch_tc32_jobs(p, nullptr, 0, stream, 0, a->path == KDA_PATH_TC_SPLIT, dump, nsc);
+}
+
+KDA_API int kda_debug_stage_floats(void) { return kda::kTc32DumpFloats; }
 
 KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const void* theta,
                             const void* beta, float g_min, float* state, float* out, int N, int H,
@@ -372,10 +410,11 @@ KDA_API const char* kda_strerror(int code) {
     case KDA_ERR_CUDA: return "CUDA runtime error";
     case KDA_ERR_UNSUPPORTED_SHAPE: return "unsupported (dtype, dk, dv) for this kernel path";
     case KDA_ERR_SCRATCH_TOO_SMALL: return "the library's scratch area cannot hold this call";
+    case KDA_ERR_BAD_SEQLENS: return "cu_seqlens is not a valid packing of the tokens";
     default: return "unknown status code";
   }
 }
 
-KDA_API int kda_version(void) { return 100; }
+KDA_API int kda_version(void) { return 200; }
 
 }  // extern "C"

@@ -27,6 +27,7 @@ struct Chain {
   int head;
   int64_t t0;   // first token row (absolute, in the flattened B*T token axis)
   int64_t t1;   // one past the last
+  bool valid;   // false: the packing table is malformed (the CTA must store nothing)
 };
 
 // Maps a chain rank to (sequence, head).  For packed variable-length batches
@@ -35,11 +36,15 @@ struct Chain {
 // blocks roughly in index order, starts the longest chains first.  Every
 // thread of the block must call this (it uses __syncthreads and `scratch`, an
 // int array of kMaxRankedSeqsDev + 1 entries in shared memory).
+// The packing table is checked where it is used: cu_seqlens[0] = 0,
+// cu_seqlens[N] = T and 0 <= t0 <= t1 <= T for this block's sequence; a block
+// whose check fails gets valid = false and an empty token range.
 __device__ __forceinline__ Chain chain_for_block(int rank_flat, int H, int N, int T,
                                                  const int32_t* cu_seqlens, int* scratch) {
   Chain c;
   int r = rank_flat / H;
   c.head = rank_flat - r * H;
+  c.valid = true;
   if (cu_seqlens == nullptr) {
     c.seq = r;
     c.t0 = (int64_t)r * T;
@@ -63,8 +68,10 @@ __device__ __forceinline__ Chain chain_for_block(int rank_flat, int H, int N, in
     __syncthreads();
   }
   c.seq = r;
-  c.t0 = cu_seqlens[r];
-  c.t1 = cu_seqlens[r + 1];
+  const int32_t a = cu_seqlens[r], b = cu_seqlens[r + 1];
+  c.valid = cu_seqlens[0] == 0 && cu_seqlens[N] == T && 0 <= a && a <= b && b <= T;
+  c.t0 = c.valid ? a : 0;
+  c.t1 = c.valid ? b : 0;
   return c;
 }
 

@@ -78,8 +78,6 @@ int launch_bwd(const BwdParams& p, cudaStream_t stream);
 int* status_word_device_ptr();
 
 int launch_simt(const FwdParams& p, cudaStream_t stream);
-int launch_tc(const FwdParams& p, cudaStream_t stream);
-bool tc_supported(int dtype, int dk, int dv);
 int launch_mma(const FwdParams& p, cudaStream_t stream);
 
 // One CTA of a segmented launch of the register-resident kernel: a token range
@@ -100,6 +98,16 @@ struct SegJob {
 int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStream_t stream,
                     uint64_t wait_ns = 0);
 
+// tcgen05/TMEM path with 32-token state steps (kda_tc32.cu): one CTA per job
+// (jobs != null) or per (sequence, head) chain.  `split_s` keeps the state's
+// bf16 copy as a high/low pair in the read-out products; `dbg` (test hook,
+// may be null) receives the stage dump of the first CTA for its first
+// `dbg_nsc` 32-token super-chunks (kTc32DumpFloats floats each).
+bool tc32_supported(int dtype, int dk, int dv);
+int launch_tc32_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStream_t stream,
+                     uint64_t wait_ns, bool split_s, float* dbg = nullptr, int dbg_nsc = 0);
+constexpr int kTc32DumpFloats = 3072 + 8192 + 128 + 32;
+
 // Segment-parallel forward (fixed-length batches, bf16, dk = dv = 128): the
 // scratch it needs and the launch sequence over a caller-provided workspace.
 size_t segmented_workspace_size(int B, int H, int T, int segments);
@@ -108,14 +116,17 @@ size_t segmented_workspace_size(int B, int H, int T, int segments);
 // device, part of the library image); null if its address cannot be found.
 constexpr size_t kNoallocScratchBytes = (size_t)KDA_NOALLOC_SCRATCH_BYTES;
 void* noalloc_scratch();
+// kernel: KDA_PATH_MMA (register-resident), KDA_PATH_TC or KDA_PATH_TC_SPLIT.
 int launch_segmented(const FwdParams& p, int segments, void* ws, size_t ws_bytes,
-                     cudaStream_t stream);
+                     cudaStream_t stream, int kernel);
 bool mma_supported(int dtype, int dk, int dv);
 
-// TMA map over a [tokens][H][128] bf16 tensor whose boxes are one chunk of 16
-// tokens x 128 channels of one head (unswizzled, out-of-range rows read 0).
-// False if the driver's encoder is unavailable or rejects the arguments.
-bool encode_token_rows(CUtensorMap* m, const void* base, int H, int64_t tokens);
+// TMA map over a [tokens][H][128] bf16 tensor whose boxes are `box_rows`
+// tokens (16: one chunk; 32: two) x 128 channels of one head (unswizzled,
+// out-of-range rows read 0).  False if the driver's encoder is unavailable or
+// rejects the arguments.
+bool encode_token_rows(CUtensorMap* m, const void* base, int H, int64_t tokens,
+                       int box_rows = kChunk);
 
 // Rank-ordered chain lookup for packed variable-length batches: blockIdx.x = r * H + h
 // runs the r-th longest sequence first (longest-processing-time order).  For

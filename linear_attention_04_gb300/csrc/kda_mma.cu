@@ -23,7 +23,7 @@
 //               chunk, with S^T (value channel x key channel) as the A operand
 //               taken straight from the fp32 accumulator registers (bf16 pairs):
 //                 [U | O] = [V^T Tb^T | 0] + S^T [-W | Qt]^T      (K = 128)
-//                 O      += U^T P^T (U as a bf16 high/low pair) + (q.k) U
+//                 O      += U^T P^T (U and P as bf16 high/low pairs) + (q.k) U
 //                 S^T    <- S^T Diag(e^{G_C}) + U^T KhC           (K = 16)
 //               then the warp writes its outputs and releases the chunk slot.
 //   warps 4..7  intra warps: warp 4+i runs chunks i, i+4, i+8, ...; each
@@ -95,8 +95,9 @@ constexpr uint32_t SL_XB = 0;                 // [32][128] bf16: rows 0..15 Kt, 
 constexpr uint32_t SL_KC = SL_XB + 2 * TILE;  // [16][128] bf16 KhC (token-major)
 constexpr uint32_t SL_V = SL_KC + TILE;       // [16][128] bf16 V (rows past the end zeroed)
 constexpr uint32_t SL_TB = SL_V + TILE;       // [16][16] bf16 Tb
-constexpr uint32_t SL_P = SL_TB + 512;        // [16][16] bf16 strictly lower P
-constexpr uint32_t SL_EGC = SL_P + 512;       // [128] fp32 e^{G_C}
+constexpr uint32_t SL_P = SL_TB + 512;        // [16][16] bf16 strictly lower P (high part)
+constexpr uint32_t SL_PL = SL_P + 512;        // [16][16] bf16 low part of P
+constexpr uint32_t SL_EGC = SL_PL + 512;      // [128] fp32 e^{G_C}
 constexpr uint32_t SL_DC = SL_EGC + 512;      // [16] fp32 q_t . k_t
 constexpr uint32_t SLOT_BYTES = SL_DC + 128;
 
@@ -224,6 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     final_state = jb.final_state;
   } else {
     ch = chain_for_block(blockIdx.x, args.H, args.N, args.T, args.cu_seqlens, (int*)(sm + SM_RANK));
+    if (!ch.valid) {
+      // malformed packing table: report it and store nothing
+      if (tid == 0) atomicExch(args.status, KDA_ERR_BAD_SEQLENS);
+      return;
+    }
     soff = ((int64_t)ch.seq * args.H + ch.head) * D * D;
   }
   // options read back from shared memory where they are used (keeps them out
@@ -427,10 +433,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_float2(s0 < g ? br0 * accA[j][0] : 0.0f, s0 + 1 < g ? br0 * accA[j][1] : 0.0f);
           *(float2*)(ab + (g + 8) * C + s0) = make_float2(
               s0 < g + 8 ? br1 * accA[j][2] : 0.0f, s0 + 1 < g + 8 ? br1 * accA[j][3] : 0.0f);
-          *(uint32_t*)(sl + SL_P + sw32(g, s0)) =
-              pack_bf16x2(s0 < g ? accP[j][0] : 0.0f, s0 + 1 < g ? accP[j][1] : 0.0f);
-          *(uint32_t*)(sl + SL_P + sw32(g + 8, s0)) =
-              pack_bf16x2(s0 < g + 8 ? accP[j][2] : 0.0f, s0 + 1 < g + 8 ? accP[j][3] : 0.0f);
+          // P as a bf16 high/low pair (P's rounding is the largest single
+          // error source of the outputs)
+          const float p0 = s0 < g ? accP[j][0] : 0.0f, p1 = s0 + 1 < g ? accP[j][1] : 0.0f;
+          const float p2 = s0 < g + 8 ? accP[j][2] : 0.0f, p3 = s0 + 1 < g + 8 ? accP[j][3] : 0.0f;
+          const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+          const __nv_bfloat162 b01 = *reinterpret_cast<const __nv_bfloat162*>(&h01);
+          const __nv_bfloat162 b23 = *reinterpret_cast<const __nv_bfloat162*>(&h23);
+          *(uint32_t*)(sl + SL_P + sw32(g, s0)) = h01;
+          *(uint32_t*)(sl + SL_P + sw32(g + 8, s0)) = h23;
+          *(uint32_t*)(sl + SL_PL + sw32(g, s0)) =
+              pack_bf16x2(p0 - __low2float(b01), p1 - __high2float(b01));
+          *(uint32_t*)(sl + SL_PL + sw32(g + 8, s0)) =
+              pack_bf16x2(p2 - __low2float(b23), p3 - __high2float(b23));
         }
       }
       __syncwarp();
@@ -605,6 +620,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma16816(accO[m][0], ul[m], pb[0], pb[1]);
           mma16816(accO[m][1], ul[m], pb[2], pb[3]);
         }
+        ldmatrix_x4(sls + SL_PL + sw32(rr + 8 * (mi >> 1), 8 * (mi & 1)), pb[0], pb[1], pb[2], pb[3]);
+#pragma unroll
+        for (int m = 0; m < kMT; ++m) {
+          mma16816(accO[m][0], uh[m], pb[0], pb[1]);
+          mma16816(accO[m][1], uh[m], pb[2], pb[3]);
+        }
       }
       // ---- S^T += U^T KhC (K = 16).  Inside the sequence U enters as bf16:
       // the outputs do not see the difference (they sum over 128 key
@@ -681,6 +702,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+constexpr int kMaxAttrDevices = 64;
+std::once_flag g_attr_once[kMaxAttrDevices];
+cudaError_t g_attr_err[kMaxAttrDevices];
+
 }  // namespace
 
 bool mma_supported(int dtype, int dk, int dv) {
@@ -701,24 +726,28 @@ int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStrea
   if (!encode_token_rows(&mq, p.q, p.H, tokens) || !encode_token_rows(&mk, p.k, p.H, tokens) ||
       !encode_token_rows(&mth, p.theta, p.H, tokens) || !encode_token_rows(&mv, p.v, p.H, tokens))
     return KDA_ERR_CUDA;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, []() {
+  // the shared-memory attribute applies to the current device's context only:
+  // set it once per device
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxAttrDevices) return KDA_ERR_CUDA;
+  std::call_once(g_attr_once[dev], [dev]() {
+    cudaError_t err = cudaSuccess;
     for (const void* fn : {(const void*)kda_fwd_mma_kernel<false>, (const void*)kda_fwd_mma_kernel<true>}) {
-      if (attr_err == cudaSuccess)
-        attr_err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-      if (kStateRegs > 0 && attr_err == cudaSuccess) {
+      if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+      if (kStateRegs > 0 && err == cudaSuccess) {
         // setmaxnreg.inc can only draw on the registers the block was launched
         // with: a split above the compiled launch allocation would wait forever
         cudaFuncAttributes fa;
-        attr_err = cudaFuncGetAttributes(&fa, fn);
-        if (attr_err == cudaSuccess &&
+        err = cudaFuncGetAttributes(&fa, fn);
+        if (err == cudaSuccess &&
             kStateWarps * kStateRegs + kIntraWarps * kIntraRegs > fa.numRegs * (kThreads / 32))
-          attr_err = cudaErrorInvalidConfiguration;
+          err = cudaErrorInvalidConfiguration;
       }
     }
+    g_attr_err[dev] = err;
   });
-  if (attr_err != cudaSuccess) return KDA_ERR_LAUNCH;
+  if (g_attr_err[dev] != cudaSuccess) return KDA_ERR_LAUNCH;
   MmaArgs a;
   a.jobs = jobs;
   a.beta = (const __nv_bfloat16*)p.beta;

@@ -22,7 +22,8 @@
 //
 // Work per chain grows by about (2P - 3) / P segment-lengths, run in parallel
 // on otherwise idle SMs.  All scratch lives in a caller-provided workspace
-// (kda_segmented_workspace_size).
+// (kda_segmented_workspace_size).  Segments are whole 32-token units, the
+// state step of the tcgen05 kernel (two 16-token chunks).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -43,15 +44,17 @@ struct SegPlan {
   size_t off_jobs1, off_jobs2, off_sst, off_sloc, off_phi, total;
 };
 
+constexpr int kSegUnit = 2 * kChunk;  // tokens per segmentation unit
+
 SegPlan plan(int B, int H, int T, int segments) {
   SegPlan s;
-  const int64_t nchunks = ((int64_t)T + kChunk - 1) / kChunk;
+  const int64_t nchunks = ((int64_t)T + kSegUnit - 1) / kSegUnit;
   int P = segments < 1 ? 1 : segments;
   if (P > nchunks) P = (int)(nchunks > 0 ? nchunks : 1);
   const int64_t per = (nchunks + P - 1) / P;  // chunks per segment
   P = (int)((nchunks + per - 1) / per);       // no empty segment
   s.P = P;
-  s.Ltok = per * kChunk;
+  s.Ltok = per * kSegUnit;
   s.NH = (int64_t)B * H;
   const int64_t n1 = s.NH * (P >= 2 ? 2 * P - 3 : 0);
   const int64_t n2 = s.NH * (P - 1);
@@ -137,9 +140,16 @@ size_t segmented_workspace_size(int B, int H, int T, int segments) {
 }
 
 int launch_segmented(const FwdParams& p, int segments, void* ws, size_t ws_bytes,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, int kernel) {
+  if ((int64_t)p.N * p.T > (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
+  const bool mma = kernel == KDA_PATH_MMA;
+  const bool split_s = kernel == KDA_PATH_TC_SPLIT;
+  auto run_jobs = [&](const FwdParams& q, const SegJob* jobs, int njobs) {
+    return mma ? launch_mma_jobs(q, jobs, njobs, stream)
+               : launch_tc32_jobs(q, jobs, njobs, stream, 0, split_s);
+  };
   const SegPlan pl = plan(p.N, p.H, p.T, segments);
-  if (pl.P < 2) return launch_mma(p, stream);
+  if (pl.P < 2) return mma ? launch_mma(p, stream) : launch_tc32_jobs(p, nullptr, 0, stream, 0, split_s);
   if (!ws || ws_bytes < pl.total) return KDA_ERR_INVALID_ARG;
   unsigned char* w = (unsigned char*)ws;
   SegJob* jobs1 = (SegJob*)(w + pl.off_jobs1);
@@ -155,13 +165,13 @@ int launch_segmented(const FwdParams& p, int segments, void* ws, size_t ws_bytes
   q.T = (int)((int64_t)p.N * p.T);
   q.N = 1;
   q.cu_seqlens = nullptr;
-  int rc = launch_mma_jobs(q, jobs1, (int)(pl.NH * (2 * pl.P - 3)), stream);
+  int rc = run_jobs(q, jobs1, (int)(pl.NH * (2 * pl.P - 3)));
   if (rc != KDA_OK) return rc;
   for (int s = 1; s <= pl.P - 2; ++s) {
     seg_combine_kernel<<<dim3((unsigned)pl.NH, D / 16), D, 0, stream>>>(sst, sloc, phi, pl.P, s);
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
   }
-  return launch_mma_jobs(q, jobs2, (int)(pl.NH * (pl.P - 1)), stream);
+  return run_jobs(q, jobs2, (int)(pl.NH * (pl.P - 1)));
 }
 
 }  // namespace kda

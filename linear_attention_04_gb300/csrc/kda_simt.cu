@@ -52,11 +52,16 @@ __global__ void __launch_bounds__(kSimtThreads)
                         const Tin* __restrict__ beta, float g_min, int gate,
                         const float* __restrict__ init_state, Tout* __restrict__ out,
                         float* __restrict__ final_state, const int32_t* __restrict__ cu_seqlens,
-                        int N, int H, int T, int dv) {
+                        int N, int H, int T, int dv, int* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SimtSmem<DK, DVS>& sm = *reinterpret_cast<SimtSmem<DK, DVS>*>(smem_raw);
   const int tid = threadIdx.x;
   const Chain ch = chain_for_block(blockIdx.x, H, N, T, cu_seqlens, sm.rank_scratch);
+  if (!ch.valid) {
+    // malformed packing table: report it and store nothing
+    if (tid == 0) atomicExch(status, KDA_ERR_BAD_SEQLENS);
+    return;
+  }
   const int h = ch.head;
   const int j0 = blockIdx.y * DVS;  // first value column of this slice
   const int64_t state_off = ((int64_t)ch.seq * H + h) * DK * dv;
@@ -220,10 +225,13 @@ int launch_simt_t(const FwdParams& p, cudaStream_t stream) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return KDA_ERR_LAUNCH;
+  int* status = status_word_device_ptr();
+  if (!status) return KDA_ERR_CUDA;
   dim3 grid((unsigned)(p.N * p.H), (unsigned)(p.dv / DVS));
   kern<<<grid, kSimtThreads, smem, stream>>>(
       (const Tin*)p.q, (const Tin*)p.k, (const Tin*)p.v, (const Tin*)p.theta, (const Tin*)p.beta,
-      p.g_min, p.gate, p.init_state, (Tout*)p.out, p.final_state, p.cu_seqlens, p.N, p.H, p.T, p.dv);
+      p.g_min, p.gate, p.init_state, (Tout*)p.out, p.final_state, p.cu_seqlens, p.N, p.H, p.T, p.dv,
+      status);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 

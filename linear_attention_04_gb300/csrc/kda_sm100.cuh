@@ -67,14 +67,25 @@ constexpr uint32_t kSleepHintNs = 100000;  // 0.1 ms per parked try_wait
 
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit_ns` of wall-clock time or as soon as *abort is set; returns false then.
+// The abort flag and the clock are read once every 16 tries.  A thread that
+// keeps waiting backs off with __nanosleep between tries (kWaitBackoffNs), so
+// that warps waiting for a hand-off leave the issue slots of their SM
+// sub-partition to the warps doing work.
+#ifndef KDA_WAIT_BACKOFF_NS
+#define KDA_WAIT_BACKOFF_NS 0
+#endif
+constexpr uint32_t kWaitBackoffNs = KDA_WAIT_BACKOFF_NS;
 KDA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
                        uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (;;) {
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if (kWaitBackoffNs > 0 && i > 2) __nanosleep(kWaitBackoffNs);
+    if ((i & 15) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
   }
 }
 

@@ -32,13 +32,13 @@ EncodeTiledFn get_encode() {
 
 }  // namespace
 
-bool encode_token_rows(CUtensorMap* m, const void* base, int H, int64_t tokens) {
+bool encode_token_rows(CUtensorMap* m, const void* base, int H, int64_t tokens, int box_rows) {
   EncodeTiledFn enc = get_encode();
   if (!enc) return false;
   constexpr int D = 128;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)tokens};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-  cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)kChunk};
+  cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

@@ -25,8 +25,9 @@ KDA_ERR_DEVICE_TIMEOUT = -5
 KDA_ERR_CUDA = -6
 KDA_ERR_UNSUPPORTED_SHAPE = -7
 KDA_ERR_SCRATCH_TOO_SMALL = -8
+KDA_ERR_BAD_SEQLENS = -9
 
-PATHS = {"auto": 0, "simt": 1, "tc": 2, "mma": 3}
+PATHS = {"auto": 0, "simt": 1, "tc": 2, "mma": 3, "tc_split": 4}
 GATES = {"sigmoid": 0, "log_decay": 1}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
@@ -97,6 +98,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, vp]
             lib.kda_chunk_fwd_ex.restype = i
             lib.kda_chunk_fwd_ex.argtypes = [ctypes.POINTER(_Args), vp]
+            lib.kda_debug_fwd_stages.restype = i
+            lib.kda_debug_fwd_stages.argtypes = [ctypes.POINTER(_Args), vp, i, vp]
+            lib.kda_debug_stage_floats.restype = i
+            lib.kda_debug_stage_floats.argtypes = []
             lib.kda_device_status.restype = i
             lib.kda_device_status.argtypes = [i]
             lib.kda_select_path.restype = i
@@ -126,6 +131,36 @@ def _stream_ptr(stream) -> int:
     return int(stream.cuda_stream)
 
 
+def _check_fwd(q, k, v, theta, beta, init_state, out, final_state, out_dtype, nseq=None):
+    """Metadata checks shared by the forward bindings (before any C call)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype = q.dtype
+    if dtype not in DTYPES:
+        raise TypeError(f"unsupported dtype {dtype}")
+    for name, t, shape in (("k", k, (B, T, H, dk)), ("theta", theta, (B, T, H, dk)),
+                           ("v", v, (B, T, H, dv)), ("beta", beta, (B, T, H))):
+        if t.dtype != dtype or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name}: expected contiguous {dtype} {shape}, got {t.dtype} "
+                             f"{tuple(t.shape)}")
+        if t.device != q.device:
+            raise ValueError(f"{name} on {t.device}, q on {q.device}")
+    if out_dtype not in DTYPES:
+        raise TypeError(f"unsupported out dtype {out_dtype}")
+    sshape = (B if nseq is None else nseq, H, dk, dv)
+    for name, t in (("init_state", init_state), ("final_state", final_state)):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != sshape or
+                              not t.is_contiguous() or t.device != q.device):
+            raise ValueError(f"{name}: expected contiguous fp32 {sshape} on {q.device}")
+    if out is not None and (out.dtype != out_dtype or tuple(out.shape) != (B, T, H, dv) or
+                            not out.is_contiguous() or out.device != q.device):
+        raise ValueError(f"out: expected contiguous {out_dtype} {(B, T, H, dv)} on {q.device}, "
+                         f"got {out.dtype} {tuple(out.shape)}")
+    if not q.is_cuda or not q.is_contiguous():
+        raise ValueError("q must be a contiguous CUDA tensor")
+    return sshape
+
+
 def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torch.Tensor,
                   beta: torch.Tensor, g_min: float = -5.0,
                   init_state: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
@@ -146,17 +181,6 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torc
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     dtype = q.dtype
-    if dtype not in DTYPES:
-        raise TypeError(f"unsupported dtype {dtype}")
-    for name, t, shape in (("k", k, (B, T, H, dk)), ("theta", theta, (B, T, H, dk)),
-                           ("v", v, (B, T, H, dv)), ("beta", beta, (B, T, H))):
-        if t.dtype != dtype or tuple(t.shape) != shape or not t.is_contiguous():
-            raise ValueError(f"{name}: expected contiguous {dtype} {shape}, got {t.dtype} "
-                             f"{tuple(t.shape)}")
-        if t.device != q.device:
-            raise ValueError(f"{name} on {t.device}, q on {q.device}")
-    if not q.is_cuda or not q.is_contiguous():
-        raise ValueError("q must be a contiguous CUDA tensor")
     nseq = B
     if cu_seqlens is not None:
         if B != 1:
@@ -164,15 +188,9 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torc
         if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
             raise ValueError("cu_seqlens must be an int32 CUDA tensor")
         nseq = cu_seqlens.numel() - 1
-    sshape = (nseq, H, dk, dv)
-    if init_state is not None:
-        if init_state.dtype != torch.float32 or tuple(init_state.shape) != sshape or \
-                not init_state.is_contiguous():
-            raise ValueError(f"init_state: expected contiguous fp32 {sshape}")
+    sshape = _check_fwd(q, k, v, theta, beta, init_state, out, final_state, out_dtype, nseq)
     if out is None:
         out = torch.empty((B, T, H, dv), dtype=out_dtype, device=q.device)
-    elif out.dtype != out_dtype or tuple(out.shape) != (B, T, H, dv) or not out.is_contiguous():
-        raise ValueError(f"out: expected contiguous {out_dtype} {(B, T, H, dv)}")
     if final_state is None and want_final_state:
         final_state = torch.empty(sshape, dtype=torch.float32, device=q.device)
     a = _Args(_ptr(q), _ptr(k), _ptr(v), _ptr(theta), _ptr(beta), float(g_min),
@@ -196,23 +214,19 @@ def kda_chunk_fwd_segmented(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                             final_state: Optional[torch.Tensor] = None, *, segments: int = 4,
                             workspace: Optional[torch.Tensor] = None,
                             want_final_state: bool = True, out_dtype: torch.dtype = torch.float32,
-                            stream=None):
+                            path: str = "auto", stream=None):
     """Segment-parallel forward through the C ABI (``kda_chunk_fwd_segmented``):
     same arguments and results as ``kda_chunk_fwd`` for a fixed-length bf16
     batch with dk = dv = 128.  ``workspace`` is a uint8 CUDA tensor of at least
-    ``kda_segmented_workspace_size`` bytes (allocated here when not given)."""
+    ``kda_segmented_workspace_size`` bytes (allocated here when not given).
+    ``path`` picks the kernel that runs the pieces ("mma", "tc_split", else tcgen05)."""
     lib = load()
     B, T, H, dk = q.shape
     dv = v.shape[-1]
-    for name, t, shape in (("k", k, (B, T, H, dk)), ("theta", theta, (B, T, H, dk)),
-                           ("v", v, (B, T, H, dv)), ("beta", beta, (B, T, H))):
-        if t.dtype != q.dtype or tuple(t.shape) != shape or not t.is_contiguous():
-            raise ValueError(f"{name}: expected contiguous {q.dtype} {shape}")
-    sshape = (B, H, dk, dv)
-    if init_state is not None and (init_state.dtype != torch.float32 or
-                                   tuple(init_state.shape) != sshape or
-                                   not init_state.is_contiguous()):
-        raise ValueError(f"init_state: expected contiguous fp32 {sshape}")
+    sshape = _check_fwd(q, k, v, theta, beta, init_state, out, final_state, out_dtype)
+    if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous() or
+                                  workspace.device != q.device):
+        raise ValueError("workspace must be a contiguous CUDA tensor on q's device")
     if out is None:
         out = torch.empty((B, T, H, dv), dtype=out_dtype, device=q.device)
     if final_state is None and want_final_state:
@@ -222,7 +236,7 @@ def kda_chunk_fwd_segmented(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     a = _Args(_ptr(q), _ptr(k), _ptr(v), _ptr(theta), _ptr(beta), float(g_min),
               _ptr(init_state), _ptr(out), _ptr(final_state), None, B, H, T, dk, dv,
-              DTYPES[q.dtype], DTYPES[out_dtype], PATHS["mma"])
+              DTYPES[q.dtype], DTYPES[out_dtype], PATHS[path])
     with torch.cuda.device(q.device):
         rc = lib.kda_chunk_fwd_segmented(ctypes.byref(a), int(segments), _ptr(workspace),
                                          workspace.numel() * workspace.element_size(), _stream_ptr(stream))
@@ -235,16 +249,24 @@ def kda_chunk_fwd_segmented_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.T
                                     theta: torch.Tensor, beta: torch.Tensor, g_min: float,
                                     init_state: Optional[torch.Tensor], out: torch.Tensor,
                                     final_state: Optional[torch.Tensor], *, segments: int = 4,
-                                    out_dtype: torch.dtype = torch.float32, stream=None):
+                                    out_dtype: Optional[torch.dtype] = None, path: str = "auto",
+                                    stream=None):
     """``kda_chunk_fwd_segmented_noalloc`` through the C ABI: the segment-parallel
     forward over the library's own scratch area.  ``out`` (and ``final_state``
-    when wanted) are caller tensors; nothing is allocated here."""
+    when wanted) are caller tensors; nothing is allocated here.  The output
+    element type is ``out.dtype`` (``out_dtype``, if given, must agree)."""
     lib = load()
     B, T, H, dk = q.shape
     dv = v.shape[-1]
+    if out is None:
+        raise ValueError("out must be given")
+    if out_dtype is not None and out_dtype != out.dtype:
+        raise ValueError(f"out_dtype {out_dtype} does not match out.dtype {out.dtype}")
+    out_dtype = out.dtype
+    _check_fwd(q, k, v, theta, beta, init_state, out, final_state, out_dtype)
     a = _Args(_ptr(q), _ptr(k), _ptr(v), _ptr(theta), _ptr(beta), float(g_min),
               _ptr(init_state), _ptr(out), _ptr(final_state), None, B, H, T, dk, dv,
-              DTYPES[q.dtype], DTYPES[out_dtype], PATHS["mma"])
+              DTYPES[q.dtype], DTYPES[out_dtype], PATHS[path])
     with torch.cuda.device(q.device):
         rc = lib.kda_chunk_fwd_segmented_noalloc(ctypes.byref(a), int(segments),
                                                  _stream_ptr(stream))
@@ -329,6 +351,43 @@ def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: to
     if rc != KDA_OK:
         raise KdaError(rc, "kda_decode_step")
     return out
+
+
+def kda_debug_fwd_stages(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torch.Tensor,
+                         beta: torch.Tensor, g_min: float = -5.0,
+                         init_state: Optional[torch.Tensor] = None, *, nsc: int = 2,
+                         gate: str = "sigmoid", path: str = "tc", stream=None):
+    """Test hook ``kda_debug_fwd_stages``: runs the tcgen05 forward and returns
+    (out, final_state, stages) where stages holds the intermediate tiles of
+    the first (sequence, head) chain for its first ``nsc`` 32-token units as
+    fp32 CPU tensors: A, P, T [nsc,32,32]; W, U [nsc,32,128]; eG [nsc,128];
+    qk [nsc,32]."""
+    lib = load()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    sshape = _check_fwd(q, k, v, theta, beta, init_state, None, None, torch.float32)
+    out = torch.empty((B, T, H, dv), dtype=torch.float32, device=q.device)
+    fin = torch.empty(sshape, dtype=torch.float32, device=q.device)
+    per = int(lib.kda_debug_stage_floats())
+    dump = torch.zeros(nsc * per, dtype=torch.float32, device=q.device)
+    a = _Args(_ptr(q), _ptr(k), _ptr(v), _ptr(theta), _ptr(beta), float(g_min),
+              _ptr(init_state), _ptr(out), _ptr(fin), None, B, H, T, dk, dv,
+              DTYPES[q.dtype], DTYPES[torch.float32], PATHS[path], GATES[gate])
+    with torch.cuda.device(q.device):
+        rc = lib.kda_debug_fwd_stages(ctypes.byref(a), _ptr(dump), int(nsc), _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_debug_fwd_stages")
+    d = dump.view(nsc, per).cpu()
+    o = 0
+    stages = {}
+    for name, shape in (("A", (32, 32)), ("P", (32, 32)), ("T", (32, 32)), ("W", (32, 128)),
+                        ("U", (32, 128)), ("eG", (128,)), ("qk", (32,))):
+        n = 1
+        for x in shape:
+            n *= x
+        stages[name] = d[:, o:o + n].reshape((nsc,) + shape)
+        o += n
+    return out, fin, stages
 
 
 def kda_device_status(clear: bool = False) -> int:

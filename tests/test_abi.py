@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_strerror_and_version():
     lib = binding.load()
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         assert lib.kda_strerror(code)
     assert lib.kda_strerror(-999) == b"unknown status code"
     assert lib.kda_version() >= 100
@@ -138,6 +138,7 @@ def test_segmented_workspace_size_host_logic():
     (dict(T=4096), dict(ws=None), binding.KDA_ERR_INVALID_ARG),
     (dict(T=4096), dict(ws=0x10010), binding.KDA_ERR_MISALIGNED),
     (dict(q=None, T=4096), {}, binding.KDA_ERR_INVALID_ARG),
+    (dict(B=1024, T=1 << 21), {}, binding.KDA_ERR_INVALID_ARG),   # B * T >= 2^31
 ])
 def test_segmented_host_side_rejection(over, extra, code):
     lib = binding.load()
@@ -155,6 +156,7 @@ def test_segmented_host_side_rejection(over, extra, code):
     (dict(cu_seqlens=0x9000), 4, binding.KDA_ERR_INVALID_ARG),
     (dict(), 0, binding.KDA_ERR_INVALID_ARG),
     (dict(g_min=0.5), 4, binding.KDA_ERR_INVALID_ARG),
+    (dict(B=1024, T=1 << 21), 2, binding.KDA_ERR_INVALID_ARG),   # B * T >= 2^31
 ])
 def test_noalloc_host_side_rejection(over, seg, code):
     lib = binding.load()
@@ -177,9 +179,13 @@ def test_gate_mode_host_checks():
     # (and stops only at the device check on a machine without a GB300)
     a = _args(gate=1, g_min=0.0)
     assert lib.kda_chunk_fwd_ex(ctypes.byref(a), None) != binding.KDA_ERR_INVALID_ARG
-    # the tcgen05 path has only the bounded gate
-    a = _args(gate=1, path=2)
-    assert lib.kda_chunk_fwd_ex(ctypes.byref(a), None) == binding.KDA_ERR_UNSUPPORTED_SHAPE
+    # every tensor-core path takes both gates; they need bf16 inputs at 128 x 128
+    for path in (2, 3, 4):
+        a = _args(gate=1, path=path)
+        assert lib.kda_chunk_fwd_ex(ctypes.byref(a), None) not in (
+            binding.KDA_ERR_INVALID_ARG, binding.KDA_ERR_UNSUPPORTED_SHAPE)
+        a = _args(path=path, dk=64, dv=64)
+        assert lib.kda_chunk_fwd_ex(ctypes.byref(a), None) == binding.KDA_ERR_UNSUPPORTED_SHAPE
 
 
 def _bwd_args(**over):
@@ -230,3 +236,43 @@ def test_selftest_hook_host_side_rejection(over, limit, ws, code):
     lib = binding.load()
     a = _args(**over)
     assert lib.kda_selftest_withheld_handoff(ctypes.byref(a), limit, ws, 256, None) == code
+
+
+@pytest.mark.parametrize("over,nsc,dump,code", [
+    (dict(), 0, 0x20000, binding.KDA_ERR_INVALID_ARG),
+    (dict(), 2, None, binding.KDA_ERR_INVALID_ARG),
+    (dict(), 2, 0x20004, binding.KDA_ERR_MISALIGNED),
+    (dict(dtype=1), 2, 0x20000, binding.KDA_ERR_UNSUPPORTED_SHAPE),
+    (dict(dk=64, dv=64), 2, 0x20000, binding.KDA_ERR_UNSUPPORTED_SHAPE),
+    (dict(T=0), 2, 0x20000, binding.KDA_ERR_INVALID_ARG),
+])
+def test_stage_dump_hook_host_side_rejection(over, nsc, dump, code):
+    lib = binding.load()
+    a = _args(**over)
+    assert lib.kda_debug_fwd_stages(ctypes.byref(a), dump, nsc, None) == code
+    assert lib.kda_debug_stage_floats() == 3 * 32 * 32 + 2 * 32 * 128 + 128 + 32
+
+
+def _cpu_inputs(B=1, T=32, H=2, d=128):
+    import torch
+    mk = lambda *s: torch.zeros(*s, dtype=torch.bfloat16)
+    return mk(B, T, H, d), mk(B, T, H, d), mk(B, T, H, d), mk(B, T, H, d), mk(B, T, H)
+
+
+def test_binding_rejects_a_mismatched_out_before_the_c_call():
+    import torch
+    q, k, v, th, be = _cpu_inputs()
+    # an out whose element type disagrees with the requested one: caught in
+    # Python, before any pointer reaches the library
+    with pytest.raises(ValueError, match="out_dtype"):
+        binding.kda_chunk_fwd_segmented_noalloc(q, k, v, th, be, -5.0, None,
+                                                torch.zeros(1, 32, 2, 128, dtype=torch.bfloat16),
+                                                None, out_dtype=torch.float32)
+    with pytest.raises(ValueError, match="out"):
+        binding.kda_chunk_fwd_segmented(q, k, v, th, be, -5.0,
+                                        out=torch.zeros(1, 16, 2, 128))
+    with pytest.raises(ValueError, match="final_state"):
+        binding.kda_chunk_fwd_segmented_noalloc(q, k, v, th, be, -5.0, None,
+                                                torch.zeros(1, 32, 2, 128), torch.zeros(1, 2, 64, 128))
+    with pytest.raises(ValueError, match="theta"):
+        binding.kda_chunk_fwd(q, k, v, th[:, :16].contiguous(), be)

@@ -37,7 +37,7 @@ def test_backward_flop_count():
 def test_source_hash_is_per_kernel():
     # each known kernel hashes its own sources; an unknown name hashes every
     # CUDA source, so the two differ
-    names = ["kda_fwd_mma_kernel", "kda_decode_kernel", "kda_bwd"]
+    names = ["kda_fwd_mma_kernel", "kda_fwd_tc32_kernel", "kda_decode_kernel", "kda_bwd"]
     hashes = {n: bench.kernel_source_hash(n) for n in names}
     assert len(set(hashes.values())) == len(names)
     assert bench.kernel_source_hash("no_such_kernel") not in hashes.values()
@@ -48,3 +48,15 @@ def test_source_hash_is_per_kernel():
 def test_fp32_alu_peak_from_unit_counts():
     # 152 SMs x 128 fp32 lanes x 2 flop per FMA x 2070 MHz
     assert bench.FP32_ALU_TFLOPS == pytest.approx(80.54784)
+
+
+def test_algorithmic_bytes_follow_the_scope_table():
+    # 1282 B per token-head at d = 128 with out at the input's 2 B, plus the
+    # fp32 final state; 1538 B with the fp32 output
+    w = bench.selected_workload(_args())
+    inp = {"lengths": [8192] * 8, "N": 8, "init_state": None}
+    th = 8 * 8192 * 32
+    state = 4 * 128 * 128 * 8 * 32
+    assert bench.algorithmic_bytes(w, inp) == th * 1282 + state
+    assert bench.algorithmic_bytes(w, inp, out_bytes=4) == th * 1538 + state
+    assert bench.algorithmic_bytes(w, inp) == 2705326080

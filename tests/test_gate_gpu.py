@@ -35,7 +35,8 @@ def _run(inp, theta, path, gate):
 
 
 @pytest.mark.parametrize("dtype,path", [(torch.float32, "simt"), (torch.bfloat16, "simt"),
-                                        (torch.bfloat16, "mma")])
+                                        (torch.bfloat16, "mma"), (torch.bfloat16, "tc"),
+                                        (torch.bfloat16, "tc_split")])
 def test_log_decay_gate_vs_oracle(dtype, path):
     # logits ~ N(2, 1): |g| ~ 2.2 per token, the decay rate of the named
     # workloads (the bf16 operand plan's error grows past the 2e-2 bar once the
@@ -44,12 +45,13 @@ def test_log_decay_gate_vs_oracle(dtype, path):
     ro, rS = oracle.fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(g), f64(inp["beta"]),
                         -5.0, None, theta_is_g=True)
     o, S = _run(inp, g, path, "log_decay")
-    tol = TOL[dtype] if path == "mma" else TOL[torch.float32]
+    tol = TOL[torch.float32] if path == "simt" else TOL[dtype]
     assert_close(f64(o), ro, tol, f"log-decay gate out ({path}, {dtype})")
     assert_close(f64(S), rS, tol, f"log-decay gate state ({path}, {dtype})")
 
 
-def test_unbounded_softplus_control():
+@pytest.mark.parametrize("path", ["mma", "tc"])
+def test_unbounded_softplus_control(path):
     # logits ~ N(8, 1): every 16-token chunk reaches -G ~ 128 > 88.7 with the
     # -softplus gate; the bounded gate on the same logits stays below 80
     inp, logits, g = _case(torch.bfloat16, mu=8.0, seed=32)
@@ -62,10 +64,10 @@ def test_unbounded_softplus_control():
                        -5.0, None, theta_is_g=True)
     assert np.all(np.isfinite(ro))
     # the dense tile path with the unbounded gate: not finite
-    o, _ = _run(inp, g, "mma", "log_decay")
+    o, _ = _run(inp, g, path, "log_decay")
     assert not bool(torch.isfinite(o).all())
     # the same logits through the bounded gate: finite and within the bar
     rb, rSb = oracle.fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(logits),
                          f64(inp["beta"]), -5.0, None)
-    ob, Sb = _run(inp, logits, "mma", "sigmoid")
+    ob, Sb = _run(inp, logits, path, "sigmoid")
     assert_close(f64(ob), rb, TOL[torch.bfloat16], "bounded gate, same logits")

@@ -20,7 +20,7 @@ def _paths(dtype, dk, dv):
         return ["simt"]
     ps = ["simt"]
     if dk == 128 and dv == 128:
-        ps += ["tc", "mma"]
+        ps += ["tc", "tc_split", "mma"]
     return ps
 
 
@@ -80,16 +80,21 @@ def _sampled(w, path, chains, seed=None):
     return inp, o, S
 
 
+# launch ranks (block index = sequence * H + head) spread over the first wave
+# (ranks 0..151 on 152 SMs) and the second (152..255)
+TRAIN_RANKS = [0, 37, 75, 118, 151, 152, 170, 199, 213, 230, 247, 255]
+
+
 @pytest.mark.parametrize("path", _bf16_paths())
 def test_train_bf16_sampled(path):
     w = WORKLOADS["train_bf16"]
-    _sampled(w, path, [(0, 0), (3, 17), (7, 31)])
+    _sampled(w, path, [(r // w.H, r % w.H) for r in TRAIN_RANKS])
 
 
 @pytest.mark.parametrize("path", _bf16_paths())
 def test_long_bf16_sampled(path):
     w = WORKLOADS["long_bf16"]
-    _sampled(w, path, [(0, 0), (0, 21)])
+    _sampled(w, path, [(0, 0), (0, 11), (0, 21), (0, 31)])
 
 
 @pytest.mark.parametrize("path", _bf16_paths())
@@ -97,9 +102,12 @@ def test_varlen_bf16_sampled(path):
     w = WORKLOADS["varlen_bf16"]
     inp = make_inputs(w, device="cpu")
     lens = inp["lengths"]
-    order = np.argsort(lens)
-    # the shortest, the longest and a middle sequence, on different heads
-    chains = [(int(order[0]), 0), (int(order[-1]), 15), (int(order[len(order) // 2]), 7)]
+    # sequences by rank in the longest-first launch order (ties by index), on
+    # different heads: the longest, the shortest and ranks in between, so that
+    # CTAs of the first, middle and last waves are checked
+    order = sorted(range(len(lens)), key=lambda i: (-lens[i], i))
+    ranks = [0, 3, 10, 21, 32, 44, 55, 63]
+    chains = [(int(order[r]), (5 * j) % w.H) for j, r in enumerate(ranks)]
     _sampled(w, path, chains)
 
 
