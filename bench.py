@@ -300,6 +300,10 @@ def run_ours(args, rank, world, local):
     q, k, v, th, be = inp["q"], inp["k"], inp["v"], inp["theta"], inp["beta"]
     init, cu = inp["init_state"], inp["cu_seqlens"]
     path = args.path if args.path != "auto" else kda_select_path(w.dtype, w.dk, w.dv)
+    gate = getattr(args, "gate", "sigmoid")
+    if gate == "log_decay":
+        # the unbounded log-decay g = -softplus(logit), drawn before timing
+        th = (-torch.nn.functional.softplus(th.float() + args.logit_mu)).to(th.dtype)
     out = torch.empty((q.shape[0], q.shape[1], w.H, w.dv), dtype=torch.float32, device=dev)
     fin = torch.empty((inp["N"], w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -318,7 +322,8 @@ def run_ours(args, rank, world, local):
                                     segments=args.segments, workspace=ws, path=seg_kernel,
                                     stream=stream)
         else:
-            kda_chunk_fwd(q, k, v, th, be, w.g_min, init, out, fin, cu, path=path, stream=stream)
+            kda_chunk_fwd(q, k, v, th, be, w.g_min, init, out, fin, cu, path=path, gate=gate,
+                          stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -439,7 +444,7 @@ def run_ours(args, rank, world, local):
                                         path=seg_kernel, stream=stream)
             else:
                 kda_chunk_fwd(dq, dk_, dv_, dth, dbe, w.g_min, b["init"], b["out"], b["fin"], cu,
-                              path=path, stream=stream)
+                              path=path, gate=gate, stream=stream)
             b["cmp"].record(stream)
             with torch.cuda.stream(s_d2h):
                 s_d2h.wait_event(b["cmp"])
@@ -480,7 +485,9 @@ def run_ours(args, rank, world, local):
             if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
             "out_dtype": "f32", "state_dtype": "f32",
             "config": {"workload": f"{w.name}: B={w.B} H={w.H} T={w.T} dk={w.dk} dv={w.dv}, "
-                                   f"chunk 16, g_min={w.g_min}, fp32 state",
+                                   f"chunk 16, g_min={w.g_min}, fp32 state" +
+                                   ("" if gate == "sigmoid" else
+                                    f", log-decay gate g = -softplus(theta + {args.logit_mu})"),
                        "B_per_gpu": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
                        "global_batch": w.B * world, "parallelism": f"sequence-shard x{world}",
                        "path": path, "seed": args.seed,
@@ -711,6 +718,10 @@ def main(argv=None):
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gate", choices=["sigmoid", "log_decay"], default="sigmoid",
+                    help="fwd: log_decay feeds g = -softplus(theta + logit_mu) (the unbounded "
+                         "parameterisation; chunks past -G = 88 take the position-wise fallback)")
+    ap.add_argument("--logit-mu", type=float, default=2.0)
     ap.add_argument("--segments", type=int, default=1,
                     help="fwd: cut each sequence into this many segments (segment-parallel path)")
     ap.add_argument("--op", choices=["fwd", "decode", "bwd"], default="fwd",

@@ -151,6 +151,141 @@ __device__ __forceinline__ void set_regs() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Largest -G2_C (log2 domain) of a chunk that the dense tile takes: e^{-G}
+// up to 2^126 stays finite in bf16 and fp32.  The bounded gate never gets
+// near it (-G_C <= 80, i.e. -G2_C <= 115.4).
+constexpr float kFallbackLog2 = 126.0f;
+
+// The position-wise form of one chunk's intra tiles, for chunks whose decay
+// is too steep for the dense product (the pages contrast it with the bounded
+// gate: "Kimi K3 Deep Dive", sections "The Problem" and "The Design").  Every
+// factor is formed per pair of positions, e^{G_r - G_s} <= 1 for s < r, so
+// nothing overflows:
+//   A_rs = b_r sum_c k_rc k_sc e^{G_rc - G_sc},   P_rs = sum_c q_rc k_sc e^{G_rc - G_sc}
+//   KhC_t = k_t e^{G_C - G_t}
+// One warp per chunk; lane l holds channels 4l .. 4l+3 (as in the dense phase
+// A).  The gate is recomputed from theta in the stage; the 120 pairs are
+// summed over the lane's channels and then over the warp, 16 pairs at a
+// time.  Writes the beta-scaled strictly lower A (fp32, 16 x 16 at `ab`), P as
+// a bf16 high/low pair and KhC into the chunk slot, replacing what the dense
+// phase A left there.
+__device__ __forceinline__ void position_wise_tiles(const unsigned char* st, unsigned char* sl, float* ab,
+                                                 int lane, float beta_l, bool log_decay, float g_min,
+                                                 f32x2 GC0, f32x2 GC1) {
+  const uint2* sk = (const uint2*)(st + 1 * TILE);
+  const uint2* sq = (const uint2*)(st + 0 * TILE);
+  const uint2* sth = (const uint2*)(st + 2 * TILE);
+  const f32x2 kL2 = f2(kLog2e, kLog2e);
+  const f32x2 kC2 = f2(-kLog2e, -kLog2e);
+  const f32x2 kC1 = f2(g_min * kLog2e, g_min * kLog2e);
+  const f32x2 kOne = f2(1.0f, 1.0f);
+  // the gate and the in-chunk cumulative sums again (log2 domain)
+  f32x2 Gl[C][2];
+  f32x2 G0 = 0ull, G1 = 0ull;
+#pragma unroll
+  for (int t = 0; t < C; ++t) {
+    const uint2 thw = sth[t * 32 + lane];
+    f32x2 g0, g1;
+    if (log_decay) {
+      g0 = mul2(bf2_to_f2(thw.x), kL2);
+      g1 = mul2(bf2_to_f2(thw.y), kL2);
+    } else {
+      const f32x2 x0 = mul2(bf2_to_f2(thw.x), kC2), x1 = mul2(bf2_to_f2(thw.y), kC2);
+      const f32x2 d0 = add2(f2(ex2_approx(f2lo(x0)), ex2_approx(f2hi(x0))), kOne);
+      const f32x2 d1 = add2(f2(ex2_approx(f2lo(x1)), ex2_approx(f2hi(x1))), kOne);
+      g0 = mul2(f2(rcp_approx(f2lo(d0)), rcp_approx(f2hi(d0))), kC1);
+      g1 = mul2(f2(rcp_approx(f2lo(d1)), rcp_approx(f2hi(d1))), kC1);
+    }
+    G0 = add2(G0, g0);
+    G1 = add2(G1, g1);
+    Gl[t][0] = G0;
+    Gl[t][1] = G1;
+  }
+  // KhC_t = k_t e^{G_C - G_t}
+#pragma unroll
+  for (int t = 0; t < C; ++t) {
+    const uint2 kw = sk[t * 32 + lane];
+    const f32x2 x0 = add2(GC0, f2(-f2lo(Gl[t][0]), -f2hi(Gl[t][0])));
+    const f32x2 x1 = add2(GC1, f2(-f2lo(Gl[t][1]), -f2hi(Gl[t][1])));
+    const f32x2 e0 = f2(ex2_approx(f2lo(x0)), ex2_approx(f2hi(x0)));
+    const f32x2 e1 = f2(ex2_approx(f2lo(x1)), ex2_approx(f2hi(x1)));
+    *(uint2*)(sl + SL_KC + sw256(t, 4 * lane)) =
+        make_uint2(f2_to_bf2(mul2(bf2_to_f2(kw.x), e0)), f2_to_bf2(mul2(bf2_to_f2(kw.y), e1)));
+  }
+  // zero the tiles (their upper parts stay zero)
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ab[8 * lane + i] = 0.0f;
+  *(uint4*)(sl + SL_P + 16 * lane) = make_uint4(0u, 0u, 0u, 0u);
+  *(uint4*)(sl + SL_PL + 16 * lane) = make_uint4(0u, 0u, 0u, 0u);
+  __syncwarp();
+  // the 120 pairs s < r, 16 at a time: lane partial sums over its channels,
+  // then a transpose-reduce over the warp (lane l ends with pair (l >> 1) & 15
+  // of the batch)
+  float pa[16], pp[16];
+  int np = 0;
+#pragma unroll
+  for (int r = 1; r < C; ++r) {
+    const uint2 kr = sk[r * 32 + lane], qr = sq[r * 32 + lane];
+    const f32x2 kr0 = bf2_to_f2(kr.x), kr1 = bf2_to_f2(kr.y);
+    const f32x2 qr0 = bf2_to_f2(qr.x), qr1 = bf2_to_f2(qr.y);
+#pragma unroll
+    for (int s2 = 0; s2 < r; ++s2) {
+      const uint2 ks = sk[s2 * 32 + lane];
+      const f32x2 x0 = add2(Gl[r][0], f2(-f2lo(Gl[s2][0]), -f2hi(Gl[s2][0])));
+      const f32x2 x1 = add2(Gl[r][1], f2(-f2lo(Gl[s2][1]), -f2hi(Gl[s2][1])));
+      const f32x2 e0 = mul2(f2(ex2_approx(f2lo(x0)), ex2_approx(f2hi(x0))), bf2_to_f2(ks.x));
+      const f32x2 e1 = mul2(f2(ex2_approx(f2lo(x1)), ex2_approx(f2hi(x1))), bf2_to_f2(ks.y));
+      const f32x2 a = fma2(kr1, e1, mul2(kr0, e0));
+      const f32x2 pq = fma2(qr1, e1, mul2(qr0, e0));
+      pa[np & 15] = f2lo(a) + f2hi(a);
+      pp[np & 15] = f2lo(pq) + f2hi(pq);
+      ++np;
+      if ((np & 15) == 0 || np == C * (C - 1) / 2) {
+        // pad a short last batch
+#pragma unroll
+        for (int z = 0; z < 16; ++z)
+          if (z >= ((np - 1) & 15) + 1) pa[z] = pp[z] = 0.0f;
+        float sa[8], sp[8], ta[4], tp[4], ua[2], up[2], va, vp;
+        const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          sa[j] = (b4 ? pa[j + 8] : pa[j]) + __shfl_xor_sync(0xffffffffu, b4 ? pa[j] : pa[j + 8], 16);
+          sp[j] = (b4 ? pp[j + 8] : pp[j]) + __shfl_xor_sync(0xffffffffu, b4 ? pp[j] : pp[j + 8], 16);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          ta[j] = (b3 ? sa[j + 4] : sa[j]) + __shfl_xor_sync(0xffffffffu, b3 ? sa[j] : sa[j + 4], 8);
+          tp[j] = (b3 ? sp[j + 4] : sp[j]) + __shfl_xor_sync(0xffffffffu, b3 ? sp[j] : sp[j + 4], 8);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          ua[j] = (b2 ? ta[j + 2] : ta[j]) + __shfl_xor_sync(0xffffffffu, b2 ? ta[j] : ta[j + 2], 4);
+          up[j] = (b2 ? tp[j + 2] : tp[j]) + __shfl_xor_sync(0xffffffffu, b2 ? tp[j] : tp[j + 2], 4);
+        }
+        va = (b1 ? ua[1] : ua[0]) + __shfl_xor_sync(0xffffffffu, b1 ? ua[0] : ua[1], 2);
+        vp = (b1 ? up[1] : up[0]) + __shfl_xor_sync(0xffffffffu, b1 ? up[0] : up[1], 2);
+        va += __shfl_xor_sync(0xffffffffu, va, 1);
+        vp += __shfl_xor_sync(0xffffffffu, vp, 1);
+        // this lane's pair index, and its (r, s) position
+        const int idx = ((np - 1) & ~15) + ((lane >> 1) & 15);
+        int pr = 1, base = 0;
+        while (base + pr <= idx) {
+          base += pr;
+          ++pr;
+        }
+        const int ps = idx - base;
+        const float br = __shfl_sync(0xffffffffu, beta_l, pr & 15);
+        if ((lane & 1) == 0 && idx < np) {
+          ab[pr * C + ps] = br * va;
+          const __nv_bfloat16 hi = __float2bfloat16_rn(vp);
+          *(__nv_bfloat16*)(sl + SL_P + sw32(pr, ps)) = hi;
+          *(__nv_bfloat16*)(sl + SL_PL + sw32(pr, ps)) = __float2bfloat16_rn(vp - __bfloat162float(hi));
+        }
+      }
+    }
+  }
+}
+
 struct MmaArgs {
   const SegJob* jobs;  // per-CTA work units (segmented launches), or null
   uint64_t wait_ns;    // limit of every bounded wait
@@ -193,14 +328,19 @@ __device__ __forceinline__ void fail(volatile int* abort, int* status) {
   atomicExch(status, KDA_ERR_DEVICE_TIMEOUT);
 }
 
-template <bool kOutBf16>
+// kFallback: compile the position-wise fallback for chunks whose decay is too
+// steep for the dense tile (only a given, unbounded log-decay can produce
+// them; the bounded gate's kernel carries no such code)
+template <bool kOutBf16, bool kFallback>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_fwd_mma_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_th,
                        const __grid_constant__ CUtensorMap tm_v, const MmaArgs args) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // pointer arithmetic on the shared array itself keeps the shared address
+  // space visible to the compiler (32-bit shared addressing)
+  unsigned char* sm = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   uint64_t* bars = (uint64_t*)(sm + SM_BARS);
   volatile int* abort = (volatile int*)(sm + SM_MISC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -392,18 +532,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
         if ((lane & 1) == 0) ((float*)(sl + SL_DC))[(lane >> 1) & 15] = v1;
       }
+      // Position-wise fallback: a chunk whose cumulative log-decay reaches
+      // -G2_C > kFallbackLog2 (only possible with a given, unbounded log-decay)
+      // would overflow e^{-G} in the dense tile; its A, P and KhC are formed
+      // from per-pair factors e^{G_r - G_s} instead (position_wise_tiles).
+      const float gmin_c = fminf(fminf(f2lo(G0), f2hi(G0)), fminf(f2lo(G1), f2hi(G1)));
+      const bool fallback = kFallback && __any_sync(0xffffffffu, !(gmin_c >= -kFallbackLog2));
       // every lane has consumed its reads of the stage: refill it with this
-      // warp's next chunk
+      // warp's next chunk (a fallback chunk reads the stage once more first)
       __syncwarp();
       if (lane == 0) KTRACE(n, 7);
-      if (n + kIntraWarps < nchunks) {
-        if (lane == 0) {
-          fence_proxy_async_smem();
-          load(n + kIntraWarps);
+      auto refill = [&]() {
+        if (n + kIntraWarps < nchunks) {
+          if (lane == 0) {
+            fence_proxy_async_smem();
+            load(n + kIntraWarps);
+          }
+          ++issued;
         }
-        ++issued;
+      };
+      if constexpr (kFallback) {
+        if (fallback) {
+          position_wise_tiles(st, sl, ab, lane, beta_l, log_decay, args.g_min, G0, G1);
+          __syncwarp();
+        }
       }
+      refill();
       // ---- phase B: A = Kt Kh^T and P = Qt Kh^T (M = N = 16, K = 128)
+      if (!fallback) {
       float accA[2][4], accP[2][4];
 #pragma unroll
       for (int j = 0; j < 2; ++j)
@@ -448,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               pack_bf16x2(p2 - __low2float(b23), p3 - __high2float(b23));
         }
       }
+      }  // dense phase B
       __syncwarp();
       if (lane == 0) KTRACE(n, 8);
       if (lane < C) {
@@ -663,6 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 dc0 = *(const float2*)(dc + 2 * q), dc1 = *(const float2*)(dc + 8 + 2 * q);
         const int nvalid = (*sflags & kJobNoOut) ? 0 : min(C, L - n * C);
         const int64_t row0 = ch.t0 + (int64_t)n * C;
+        {
 #pragma unroll
         for (int m = 0; m < kMT; ++m)
 #pragma unroll
@@ -681,6 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   ((float*)args.out)[idx] = o;
               }
             }
+        }
       }
       // the slot's reads are all consumed (their values fed the products above)
       __syncwarp();
@@ -732,7 +891,8 @@ int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStrea
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxAttrDevices) return KDA_ERR_CUDA;
   std::call_once(g_attr_once[dev], [dev]() {
     cudaError_t err = cudaSuccess;
-    for (const void* fn : {(const void*)kda_fwd_mma_kernel<false>, (const void*)kda_fwd_mma_kernel<true>}) {
+    for (const void* fn : {(const void*)kda_fwd_mma_kernel<false, false>, (const void*)kda_fwd_mma_kernel<true, false>,
+                           (const void*)kda_fwd_mma_kernel<false, true>, (const void*)kda_fwd_mma_kernel<true, true>}) {
       if (err == cudaSuccess)
         err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
       if (kStateRegs > 0 && err == cudaSuccess) {
@@ -766,10 +926,15 @@ int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStrea
   if (!a.status) return KDA_ERR_CUDA;
   const unsigned grid = jobs ? (unsigned)njobs : (unsigned)(p.N * p.H);
   if (grid == 0) return KDA_OK;
-  if (a.out_bf16)
-    kda_fwd_mma_kernel<true><<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
+  const bool fb = p.gate == KDA_GATE_LOG_DECAY;
+  if (a.out_bf16 && fb)
+    kda_fwd_mma_kernel<true, true><<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
+  else if (a.out_bf16)
+    kda_fwd_mma_kernel<true, false><<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
+  else if (fb)
+    kda_fwd_mma_kernel<false, true><<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
   else
-    kda_fwd_mma_kernel<false><<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
+    kda_fwd_mma_kernel<false, false><<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 

@@ -3,7 +3,10 @@ unbounded -softplus control: with g = -softplus(theta) the in-chunk factor
 e^{-G} overflows once the logits are large, so the dense tile products stop
 being finite, while the bounded gate g_min * sigmoid(theta) on the very same
 logits never leaves e^{80} ("Architecture Deep Dive", sec. 3.2; "Kimi K3 Deep
-Dive", section "The Design")."""
+Dive", section "The Design").  The register-resident path detects such chunks
+and forms their tiles position by position (per-pair e^{G_r - G_s}), so its
+results stay finite and within the bar; the tcgen05 path has no such
+fallback and is the control."""
 import numpy as np
 import pytest
 import torch
@@ -60,14 +63,34 @@ def test_unbounded_softplus_control(path):
     gs = -5.0 * torch.sigmoid(logits.double())
     assert float((-gs.reshape(2, -1, 16, 3, 128).sum(dim=2)).max()) <= 80.0
     # the fp64 oracle is finite either way
-    ro, _ = oracle.fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(g), f64(inp["beta"]),
-                       -5.0, None, theta_is_g=True)
+    ro, rS = oracle.fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(g), f64(inp["beta"]),
+                        -5.0, None, theta_is_g=True)
     assert np.all(np.isfinite(ro))
-    # the dense tile path with the unbounded gate: not finite
-    o, _ = _run(inp, g, path, "log_decay")
-    assert not bool(torch.isfinite(o).all())
+    o, S = _run(inp, g, path, "log_decay")
+    if path == "tc":
+        # the dense tile path with the unbounded gate: not finite
+        assert not bool(torch.isfinite(o).all())
+    else:
+        # every chunk takes the position-wise fallback: finite and within the bar
+        assert_close(f64(o), ro, TOL[torch.bfloat16], "position-wise fallback out")
+        assert_close(f64(S), rS, TOL[torch.bfloat16], "position-wise fallback state")
     # the same logits through the bounded gate: finite and within the bar
     rb, rSb = oracle.fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(logits),
                          f64(inp["beta"]), -5.0, None)
     ob, Sb = _run(inp, logits, path, "sigmoid")
     assert_close(f64(ob), rb, TOL[torch.bfloat16], "bounded gate, same logits")
+
+
+def test_fallback_on_some_chunks_only():
+    """logits ~ N(4.75, 1): some 16-token chunks (about a fifth) pass the dense tile's limit
+    (-G = 126 / log2 e = 87.3 on any channel) and some do not, so the
+    register-resident path mixes dense and position-wise chunks in one chain."""
+    inp, _, g = _case(torch.bfloat16, mu=4.75, seed=33, T=640)
+    G = (-g.double()).reshape(2, -1, 16, 3, 128).sum(dim=2).amax(dim=-1)  # per chunk and head
+    share = float((G > 126.0 / 1.4426950408889634).double().mean())
+    assert 0.05 < share < 0.99
+    ro, rS = oracle.fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(g), f64(inp["beta"]),
+                        -5.0, None, theta_is_g=True)
+    o, S = _run(inp, g, "mma", "log_decay")
+    assert_close(f64(o), ro, TOL[torch.bfloat16], "mixed fallback out")
+    assert_close(f64(S), rS, TOL[torch.bfloat16], "mixed fallback state")
