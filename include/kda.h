@@ -56,7 +56,7 @@
  *
  * Errors: every entry point returns KDA_OK (0) or a negative KDA_ERR_* code
  * and never throws.  Argument errors are found on the host before anything
- * is queued.  A device-side wait that runs out (the tensor-core path bounds
+ * is queued.  A device-side wait that runs out (the tensor-core paths bound
  * every wait) records KDA_ERR_DEVICE_TIMEOUT in a per-device status word that
  * kda_device_status() reads after the caller has synchronised.
  */
@@ -149,11 +149,15 @@ KDA_API int kda_chunk_fwd_f32(const float* q, const float* k, const float* v, co
  * `gate` selects how theta becomes the log-decay.  KDA_GATE_SIGMOID is the
  * bounded gate of the pages, under which every in-chunk factor e^{-G} stays
  * at or below e^{80}.  KDA_GATE_LOG_DECAY takes g from theta as given (any
- * g <= 0, for instance -softplus of a logit) with no bound: the tensor-core
- * paths then need the sum of |g| over every 16-token chunk (chunks counted
- * from the sequence start) to stay below about 88 (fp32 and bf16 overflow of
- * e^{-G}), else their results are not finite; the SIMT path has the same
- * limit. */
+ * g <= 0, for instance -softplus of a logit) with no bound.  The
+ * register-resident path (KDA_PATH_MMA, the AUTO choice for bf16 at
+ * dk = dv = 128) then forms the tiles of every 16-token chunk whose sum of
+ * |g| passes 126 ln 2 (about 87.3) position by position, from per-pair
+ * factors e^{G_r - G_s} <= 1, so its results stay finite for any g <= 0; such
+ * chunks cost several times a dense chunk.  The tcgen05 paths and the SIMT
+ * path have no such fallback: they need the sum of |g| over every 16-token
+ * chunk (chunks counted from the sequence start) to stay below about 88
+ * (fp32 and bf16 overflow of e^{-G}), else their results are not finite. */
 typedef struct kda_fwd_args {
   const void* q;
   const void* k;
