@@ -221,8 +221,8 @@ KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* args, int segments, void
  * written).  `dtype` (KDA_DTYPE_*) is the type of q, k, v, theta, beta; every
  * gradient and d_out/d_final are fp32.  `gate` as kda_fwd_args.gate.
  * `workspace`: device memory of kda_chunk_bwd_workspace_size(B, H, T, dk, dv)
- * bytes (B * H * ceil(T / 16) * 136 KB: two fp32 128 x 128 states and a
- * 16 x 128 fp32 tile per chunk), 16-byte aligned, caller-owned, scratch until
+ * bytes (B * H * ceil(T / 16) * 152 KB: two fp32 128 x 128 states and three
+ * 16 x 128 fp32 tiles per chunk), 16-byte aligned, caller-owned, scratch until
  * the stream has passed the call; it needs no initial contents.  The library
  * allocates nothing.  A given log-decay (KDA_GATE_LOG_DECAY) has the forward
  * pass's limit: the in-chunk sum of |g| below about 88.  Returns KDA_OK or

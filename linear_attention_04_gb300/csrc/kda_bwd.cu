@@ -55,6 +55,7 @@ constexpr int TILE_F = C * LD;        // floats of a token tile
 constexpr int STATE_F = D * LD;       // floats of the padded state
 constexpr int SM16_F = C * LS;        // floats of a 16 x 16 matrix
 constexpr size_t kStateF = (size_t)D * D;  // floats of one state in the workspace
+static_assert(5 * SM16_F <= 4 * TILE_F, "inverse scratch fits the partial-sum tiles");
 
 struct BwdDev {
   const void* q;
@@ -76,8 +77,25 @@ struct BwdDev {
   float* ws_S;   // [chain][chunk][128][128] state at each chunk start
   float* ws_dS;  // [chain][chunk][128][128] gradient w.r.t. each chunk's end state
   float* ws_dU;  // [chain][chunk][16][128]
+  float* ws_RU;  // [chain][chunk][2][16][128]: R = V - Kt S and U = Tb R of each chunk
   int H, T, nch;
 };
+
+// d0 += a * b0 and d1 += a * b1 as one packed instruction: two IEEE fp32
+// fused multiply-adds, bit-identical to two fmaf calls, in one issue slot.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a, float b0, float b1) {
+  asm("{\n .reg .b64 pa, pb, pd;\n mov.b64 pa, {%2, %2};\n mov.b64 pb, {%3, %4};\n"
+      " mov.b64 pd, {%0, %1};\n fma.rn.f32x2 pd, pa, pb, pd;\n mov.b64 {%0, %1}, pd;\n}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a), "f"(b0), "f"(b1));
+}
+// d0 += a0 * b0 and d1 += a1 * b1 as one packed instruction.
+__device__ __forceinline__ void ffma2v(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 pa, pb, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n"
+      " mov.b64 pd, {%0, %1};\n fma.rn.f32x2 pd, pa, pb, pd;\n mov.b64 {%0, %1}, pd;\n}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
 
 // acc[m][t] += sum_{k0 <= k < k1} A(m0 + m, k) B(k, col(t)), operands in shared
 // memory.  A: A[m * lda + k] (AMK) or A[k * lda + m].  B: BKN -> B[k * ldb +
@@ -90,6 +108,7 @@ __device__ __forceinline__ void gemm_acc(float (&acc)[TM][TN], const float* A, i
                                          int k1) {
   static_assert(AMK || TM % 4 == 0, "k-major A needs TM % 4 == 0");
   static_assert(!BKN || TN % 4 == 0, "k-major B needs TN % 4 == 0");
+  static_assert(TN % 2 == 0, "column pairs");
   for (int k = k0; k < k1; k += 4) {
     float a[TM][4], b[4][TN];
     if constexpr (AMK) {
@@ -139,7 +158,17 @@ __device__ __forceinline__ void gemm_acc(float (&acc)[TM][TN], const float* A, i
 #pragma unroll
       for (int m = 0; m < TM; ++m)
 #pragma unroll
-        for (int t = 0; t < TN; ++t) acc[m][t] = fmaf(a[m][kk], b[kk][t], acc[m][t]);
+        for (int t = 0; t < TN; t += 2) {
+          if constexpr (BKN) {
+            // column pairs straight from the float4 loads of B: one packed
+            // instruction per pair
+            ffma2(acc[m][t], acc[m][t + 1], a[m][kk], b[kk][t], b[kk][t + 1]);
+          } else {
+            // columns from separate loads would need packing: scalar FMAs
+            acc[m][t] = fmaf(a[m][kk], b[kk][t], acc[m][t]);
+            acc[m][t + 1] = fmaf(a[m][kk], b[kk][t + 1], acc[m][t + 1]);
+          }
+        }
   }
 }
 
@@ -234,70 +263,103 @@ __device__ __forceinline__ void small16(const float* A, const float* B, float* o
   }
 }
 
-// sum_k X[m][k] Y[n][k] over the 128 channels of two token tiles.
+// sum_k X[m][k] Y[n][k] over the 128 channels of two token tiles, in four
+// independent partial sums (k mod 4) added at the end.
 __device__ __forceinline__ float dot128(const float* X, int m, const float* Y, int n) {
-  float acc[1][1] = {{0.0f}};
-  gemm_acc<1, 1, true, false>(acc, X, LD, m, Y, LD, n, 0, 0, D);
-  return acc[0][0];
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  const float* x = X + m * LD;
+  const float* y = Y + n * LD;
+#pragma unroll 8
+  for (int k = 0; k < D; k += 4) {
+    const float4 a = *(const float4*)(x + k), b = *(const float4*)(y + k);
+    ffma2v(acc[0], acc[1], a.x, a.y, b.x, b.y);
+    ffma2v(acc[2], acc[3], a.z, a.w, b.z, b.w);
+  }
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
-// The chunk's operands from q, k, theta (threads 0..127: one channel each,
-// sequential over the 16 tokens), v and beta (threads 128..255).  Element
-// (t, c) of theta is th0[t * rs + c], and so on for k, q and v: rows of the
-// global tensors (rs = H * D) or of a staged copy in shared memory (rs = D).
-// Thread 128 + t (t < 16) passes beta_t in bval.  The decay factors are
-// running products of the per-token factors e^{g}: e^{G_t} = prod_{s <= t}
-// e^{g_s}, e^{-G_t} = prod_{s <= t} 1 / e^{g_s} and e^{G_C - G_t} =
-// prod_{s > t} e^{g_s}.  (The exponential of an fp32 cumulative sum would
-// carry the sum's rounding, up to half an ulp of |G| <= 80 per step, into
-// every factor; the products stay within a few ulp.)  Rows past the sequence
-// end are neutral (q = k = v = 0, g = 0, beta = 0).  Null outputs are
-// skipped.  Kt is written times ksign; EGt receives e^{g}.
+// The chunk's operands in two passes over all threads.  Element (t, c) of
+// theta is th0[t * rs + c], and so on for k, q and v: rows of the global
+// tensors (rs = H * D) or of a staged copy in shared memory (rs = D).
+//   pass 1 (thread -> channel c = tid % 128, tokens 8 (tid / 128) .. + 7):
+//     every load of the chunk, the gate g, its derivative factor dg and the
+//     per-token factors e^{g} and 1 / e^{g}; V is written, and the raw k and q
+//     wait in the KhC and Qt tiles;
+//   pass 2 (threads 0..127, one channel each, sequential over the 16
+//     tokens): the decay factors as running products, e^{G_t} =
+//     prod_{s <= t} e^{g_s}, e^{-G_t} = prod_{s <= t} 1 / e^{g_s} and
+//     e^{G_C - G_t} = prod_{s > t} e^{g_s}.  (The exponential of an fp32
+//     cumulative sum would carry the sum's rounding, up to half an ulp of
+//     |G| <= 80 per step, into every factor; the products stay within a few
+//     ulp.)
+// Thread 128 + t (t < 16) passes beta_t in bval.  Rows past the sequence end
+// are neutral (q = k = v = 0, g = 0, beta = 0).  Null outputs are skipped.
+// Kt is written times ksign; EGt receives e^{g}.  Contains a __syncthreads:
+// every thread of the CTA calls it.
 template <typename Tin>
 __device__ __forceinline__ void load_chunk(const Tin* th0, const Tin* k0, const Tin* q0,
                                            const Tin* v0, int64_t rs, float bval, float g_min,
                                            int log_decay, int nvalid, float* Qt, float* Kt,
                                            float ksign, float* Kh, float* KhC, float* EGt,
                                            float* dgt, float* ec, float* bt, float* V) {
+  constexpr int CH = C / 2;
   const int tid = threadIdx.x;
-  if (tid < D) {
-    const int c = tid;
-    // every load of the chunk first (independent, so they overlap), then the
-    // sequential pass over the tokens
-    float xr[C], kr[C], qr[C], egr[C];
+  if (tid < 2 * D) {
+    const int c = tid & (D - 1), tb = (tid >> 7) * CH;
+    float xr[CH], kr[CH], qr[CH], vr[CH];
 #pragma unroll
-    for (int t = 0; t < C; ++t) {
+    for (int i = 0; i < CH; ++i) {
+      const int t = tb + i;
       const bool ok = t < nvalid;
-      xr[t] = ok ? to_f32(th0[t * rs + c]) : 0.0f;
-      kr[t] = ok ? to_f32(k0[t * rs + c]) : 0.0f;
-      qr[t] = (ok && Qt) ? to_f32(q0[t * rs + c]) : 0.0f;
+      xr[i] = ok ? to_f32(th0[t * rs + c]) : 0.0f;
+      kr[i] = ok ? to_f32(k0[t * rs + c]) : 0.0f;
+      qr[i] = (ok && Qt) ? to_f32(q0[t * rs + c]) : 0.0f;
+      vr[i] = (ok && V) ? to_f32(v0[t * rs + c]) : 0.0f;
     }
-    float E = 1.0f, Ei = 1.0f;
 #pragma unroll
-    for (int t = 0; t < C; ++t) {
-      const float kv = kr[t], qv = qr[t], x = xr[t];
+    for (int i = 0; i < CH; ++i) {
+      const int t = tb + i;
       float g = 0.0f, dg = 0.0f;
       if (t < nvalid) {
         if (log_decay) {
-          g = x;
+          g = xr[i];
           dg = 1.0f;
         } else {
-          // sigmoid(x) and sigmoid(-x) each from its own exponential: their
-          // product keeps full relative precision where one of them is near 1
-          const float sp = 1.0f / (1.0f + expf(-x)), sn = 1.0f / (1.0f + expf(x));
+          // sigmoid(x) and sigmoid(-x) from one exponential of -|x|: both
+          // keep full relative precision (neither is formed as 1 - the other)
+          const float x = xr[i];
+          const float e = expf(-fabsf(x));
+          const float big = 1.0f / (1.0f + e), small = e * big;
+          const float sp = x >= 0.0f ? big : small, sn = x >= 0.0f ? small : big;
           g = g_min * sp;
           dg = g_min * sp * sn;
         }
       }
       const float eg = expf(g);
-      E *= eg;
-      Ei *= 1.0f / eg;
-      egr[t] = eg;
-      Kt[t * LD + c] = ksign * kv * E;
-      Kh[t * LD + c] = kv * Ei;
-      if (Qt) Qt[t * LD + c] = qv * E;
+      Kt[t * LD + c] = eg;
+      Kh[t * LD + c] = 1.0f / eg;
+      KhC[t * LD + c] = kr[i];
+      if (Qt) Qt[t * LD + c] = qr[i];
+      if (V) V[t * LD + c] = vr[i];
       if (EGt) EGt[t * LD + c] = eg;
       if (dgt) dgt[t * LD + c] = dg;
+    }
+  }
+  __syncthreads();
+  if (tid < D) {
+    const int c = tid;
+    float kr[C], egr[C];
+    float E = 1.0f, Ei = 1.0f;
+#pragma unroll
+    for (int t = 0; t < C; ++t) {
+      kr[t] = KhC[t * LD + c];
+      const float eg = Kt[t * LD + c];
+      E *= eg;
+      Ei *= Kh[t * LD + c];
+      egr[t] = eg;
+      Kt[t * LD + c] = ksign * kr[t] * E;
+      Kh[t * LD + c] = kr[t] * Ei;
+      if (Qt) Qt[t * LD + c] *= E;
     }
     ec[c] = E;
     float P = 1.0f;
@@ -306,16 +368,8 @@ __device__ __forceinline__ void load_chunk(const Tin* th0, const Tin* k0, const 
       KhC[t * LD + c] = kr[t] * P;
       P *= egr[t];
     }
-  } else if (tid < 2 * D) {
-    const int c = tid - D;
-    if (V) {
-      float vr[C];
-#pragma unroll
-      for (int t = 0; t < C; ++t) vr[t] = t < nvalid ? to_f32(v0[t * rs + c]) : 0.0f;
-#pragma unroll
-      for (int t = 0; t < C; ++t) V[t * LD + c] = vr[t];
-    }
-    if (c < C) bt[c] = bval;
+  } else if (tid < D + C) {
+    bt[tid - D] = bval;
   }
 }
 
@@ -369,29 +423,68 @@ __device__ __forceinline__ void load_dout(const BwdDev& a, int64_t row0, int h, 
   }
 }
 
-// M = (I + Diag(b) Ab)^{-1} by forward substitution (thread j < 16: column j),
-// Tb = M Diag(b), and the transpose of Tb when asked.
+// M = (I + N)^{-1} with N = Diag(b) Ab strictly lower, Tb = M Diag(b), and the
+// transpose of Tb when asked.  N is nilpotent (N^16 = 0), so
+//   (I + N)^{-1} = (I - N)(I + N^2)(I + N^4)(I + N^8),
+// four rounds of 16 x 16 products instead of sixteen sequential substitution
+// steps: every thread (i, j) = (tid / 16, tid % 16) forms entry (i, j) of each
+// product.  `scratch` holds five 16 x 16 matrices.  Contains __syncthreads:
+// every thread of the CTA calls it; M, Tb and TbT are complete after the
+// caller's next barrier.
 __device__ __forceinline__ void wy_inverse(const float* Ab, const float* bt, float* M, float* Tb,
-                                           float* TbT) {
-  const int j = threadIdx.x;
-  if (j >= C) return;
-  float t[C];
+                                           float* TbT, float* scratch) {
+  const int i = threadIdx.x >> 4, j = threadIdx.x & 15;
+  const int ij = i * LS + j;
+  float* B0 = scratch;
+  float* B1 = B0 + SM16_F;
+  float* B2 = B1 + SM16_F;
+  float* B3 = B2 + SM16_F;
+  float* B4 = B3 + SM16_F;
+  // B0 = N, B1 = I - N
+  const float n = j < i ? bt[i] * Ab[ij] : 0.0f;
+  B0[ij] = n;
+  B1[ij] = (i == j ? 1.0f : 0.0f) - n;
+  __syncthreads();
+  // B2 = N^2
+  {
+    float x = 0.0f;
 #pragma unroll
-  for (int i = 0; i < C; ++i) t[i] = (i == j) ? 1.0f : 0.0f;
-#pragma unroll
-  for (int i = 1; i < C; ++i) {
-    float acc = 0.0f;
-#pragma unroll
-    for (int l = 0; l < i; ++l) acc = fmaf(Ab[i * LS + l], t[l], acc);
-    if (i > j) t[i] = -bt[i] * acc;
+    for (int l = 0; l < C; ++l) x = fmaf(B0[i * LS + l], B0[l * LS + j], x);
+    B2[ij] = x;
   }
+  __syncthreads();
+  // B3 = (I - N)(I + N^2), B4 = N^4
+  {
+    float q = B1[ij], x = 0.0f;
+#pragma unroll
+    for (int l = 0; l < C; ++l) {
+      q = fmaf(B1[i * LS + l], B2[l * LS + j], q);
+      x = fmaf(B2[i * LS + l], B2[l * LS + j], x);
+    }
+    B3[ij] = q;
+    B4[ij] = x;
+  }
+  __syncthreads();
+  // B1 = B3 (I + N^4), B0 = N^8
+  {
+    float q = B3[ij], x = 0.0f;
+#pragma unroll
+    for (int l = 0; l < C; ++l) {
+      q = fmaf(B3[i * LS + l], B4[l * LS + j], q);
+      x = fmaf(B4[i * LS + l], B4[l * LS + j], x);
+    }
+    B1[ij] = q;
+    B0[ij] = x;
+  }
+  __syncthreads();
+  // M = B1 (I + N^8)
+  float q = B1[ij];
+#pragma unroll
+  for (int l = 0; l < C; ++l) q = fmaf(B1[i * LS + l], B0[l * LS + j], q);
   const float bj = bt[j];
-#pragma unroll
-  for (int i = 0; i < C; ++i) {
-    M[i * LS + j] = t[i];
-    Tb[i * LS + j] = t[i] * bj;
-    if (TbT) TbT[j * LS + i] = t[i] * bj;
-  }
+  M[ij] = q;
+  Tb[ij] = q * bj;
+  if (TbT) TbT[j * LS + i] = q * bj;
 }
 
 // Thread tile of the register-resident 128 x 128 state: element [i][4 g + c]
@@ -469,12 +562,12 @@ __device__ __forceinline__ void states_chain(const BwdDev& a, int64_t chain) {
     return load_beta<Tin>(a, r0, h, nv);
   };
 
+  float* RUw = a.ws_RU + (size_t)chain * a.nch * 2 * C * D;
   float st[8][8];
   state_load(st, a.init_state ? a.init_state + chain * kStateF : nullptr);
-  float bnext = a.nch > 1 ? stage(0) : 0.0f;
+  float bnext = stage(0);
   for (int n = 0; n < a.nch; ++n) {
     state_store(st, Sw + (size_t)n * kStateF, D);
-    if (n + 1 == a.nch) break;  // the last chunk's end state is not needed
     state_store(st, S, LD);
     const int t0 = n * C, nvalid = min(C, a.T - t0);
     cp_async_wait_all();
@@ -482,19 +575,28 @@ __device__ __forceinline__ void states_chain(const BwdDev& a, int64_t chain) {
     load_chunk<Tin>(sth, sk, nullptr, sv, D, bnext, a.g_min, a.log_decay, nvalid, nullptr, Kt,
                     1.0f, Kh, KhC, nullptr, nullptr, ec, bt, V);
     __syncthreads();
-    if (n + 2 < a.nch) bnext = stage(n + 1);  // overlaps this chunk's products
+    if (n + 1 < a.nch) bnext = stage(n + 1);  // overlaps this chunk's products
     {
       const int m = tid >> 4, nn = tid & 15;
       Ab[m * LS + nn] = nn < m ? dot128(Kt, m, Kh, nn) : 0.0f;
     }
+    __syncthreads();
+    wy_inverse(Ab, bt, M, Tb, nullptr, part);  // (the partial sums' tiles are free here)
+    __syncthreads();
     part16<true>(Kt, S, part);  // Kt S
     __syncthreads();
-    wy_inverse(Ab, bt, M, Tb, nullptr);
     reduce_parts<C, 4>(part, V, V, -1.0f);  // R = V - Kt S
     __syncthreads();
     small16<false>(Tb, V, U, 1.0f);  // U = Tb R
     __syncthreads();
-    state_update<C>(st, ec, KhC, U);  // S' = Diag(ec) S + KhC^T U
+    // R and U of the chunk for the gradient kernel
+    for (int e = tid; e < 2 * C * D / 4; e += kThreads) {
+      const int t = (e >> 5) & (C - 1), c = (e & 31) * 4;
+      const float* src = (e < C * D / 4 ? V : U) + t * LD + c;
+      *(float4*)(RUw + (size_t)n * 2 * C * D + (e >> 5) * D + c) = *(const float4*)src;
+    }
+    // the last chunk's end state is not needed
+    if (n + 1 < a.nch) state_update<C>(st, ec, KhC, U);  // S' = Diag(ec) S + KhC^T U
   }
 }
 
@@ -558,9 +660,10 @@ __device__ __forceinline__ void reverse_chain(const BwdDev& a, int64_t chain) {
       Ab[m * LS + nn] = nn < m ? -dot128(mKt, m, Kh, nn) : 0.0f;
       PiT[nn * LS + m] = nn <= m ? dot128(Qt, m, Kh, nn) : 0.0f;
     }
-    part16<true>(KhC, dS, part);  // KhC dS'
     __syncthreads();
-    wy_inverse(Ab, bt, M, Tb, TbT);
+    wy_inverse(Ab, bt, M, Tb, TbT, part);  // (the partial sums' tiles are free here)
+    __syncthreads();
+    part16<true>(KhC, dS, part);  // KhC dS'
     small16<false>(PiT, dO, dU, 1.0f);  // Pi^T dO
     __syncthreads();
     reduce_parts<C, 4>(part, dU, dU, 1.0f);  // dU = Pi^T dO + KhC dS'
@@ -638,21 +741,27 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
   const float* Sg = a.ws_S + cidx * kStateF;
   const float* dSg = a.ws_dS + cidx * kStateF;
   const float* dUg = a.ws_dU + cidx * C * D;
+  const float* RUg = a.ws_RU + cidx * 2 * C * D;
 
   // ---- operands of the chunk, S, dO and dU
   {
     const int64_t g0 = (row0 * a.H + h) * D;
     load_chunk<Tin>((const Tin*)a.theta + g0, (const Tin*)a.k + g0, (const Tin*)a.q + g0,
                     (const Tin*)a.v + g0, (int64_t)a.H * D, load_beta<Tin>(a, row0, h, nvalid),
-                    a.g_min, a.log_decay, nvalid, Qt, Kt, 1.0f, Kh, KhC, EGt, dgt, ec, bt, V);
+                    a.g_min, a.log_decay, nvalid, Qt, Kt, 1.0f, Kh, KhC, EGt, dgt, ec, bt, nullptr);
   }
   load_dout(a, row0, h, nvalid, X);
   {
-    float4 u[2], x[16];
+    float4 u[2], ru[4], x[16];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int e = tid + i * kThreads;
       u[i] = *(const float4*)(dUg + (e >> 5) * D + (e & 31) * 4);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = tid + i * kThreads;
+      ru[i] = *(const float4*)(RUg + (e >> 5) * D + (e & 31) * 4);
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -663,6 +772,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
     for (int i = 0; i < 2; ++i) {
       const int e = tid + i * kThreads;
       *(float4*)(dU + (e >> 5) * LD + (e & 31) * 4) = u[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // R into the V tile, U into the U tile
+      const int e = tid + i * kThreads;
+      *(float4*)((i < 2 ? V : U) + ((e >> 5) & (C - 1)) * LD + (e & 31) * 4) = ru[i];
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -680,12 +795,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
     Ab[m * LS + nn] = nn < m ? dot128(Kt, m, Kh, nn) : 0.0f;
     Pi[m * LS + nn] = nn <= m ? dot128(Qt, m, Kh, nn) : 0.0f;
   }
-  part16<true>(Kt, S, part);  // Kt S
   __syncthreads();
-  wy_inverse(Ab, bt, M, Tb, TbT);
-  reduce_parts<C, 4>(part, V, V, -1.0f);  // R = V - Kt S
+  wy_inverse(Ab, bt, M, Tb, TbT, part);  // (the partial sums' tiles are free here)
   __syncthreads();
-  small16<false>(Tb, V, U, 1.0f);              // U = Tb R
   small16<false>(TbT, dU, X + TILE_F, -1.0f);  // -dR = -Tb^T dU
   __syncthreads();
   {
@@ -769,53 +881,89 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
   // sum_t dKhC_t KhC_t (through dG_C); they are summed in the equal closed
   // form sum_{t < s} dKhC_t KhC_t, which avoids cancelling two large sums when
   // the last tokens' terms dominate (fast decay).
-  if (tid < D) {
-    const int c = tid;
-    // the decay factors again, by the same products as in load_chunk
-    float sfx[C];  // e^{G_C - G_t}
-    float P = 1.0f;
-#pragma unroll
-    for (int t = C - 1; t >= 0; --t) {
-      sfx[t] = P;
-      P *= EGt[t * LD + c];
-    }
-    float qr[C], kr[C];
-#pragma unroll
-    for (int t = 0; t < C; ++t) {
-      const int64_t o = ((row0 + t) * a.H + h) * D + c;
-      qr[t] = t < nvalid ? to_f32(((const Tin*)a.q)[o]) : 0.0f;
-      kr[t] = t < nvalid ? to_f32(((const Tin*)a.k)[o]) : 0.0f;
-    }
-    float E = 1.0f, Ei = 1.0f;
-    float dG[C], pre[C];
+  // Two threads per channel: thread (c, half) takes tokens 8 half .. 8 half + 7.
+  // The running products and sums that cross the two halves go through
+  // shared memory (the dead partial-sum tiles), each formed in the order of
+  // one sequential pass, so the results equal that pass bit for bit.
+  constexpr int CH = C / 2;
+  const int c = tid & (D - 1), hf = tid >> 7, tb = hf * CH;
+  float* xs = part;  // [5][D]: E and e^{-G} after token 7, prefix sum, suffix product, suffix sum
+  float egl[CH], dG[CH];
+  {
     float run = 0.0f;
 #pragma unroll
-    for (int t = 0; t < C; ++t) {
-      const float eg = EGt[t * LD + c];
-      E *= eg;
-      Ei *= 1.0f / eg;
+    for (int i = 0; i < CH; ++i) {
+      const int t = tb + i;
+      egl[i] = EGt[t * LD + c];
+      const float dqt = X[t * LD + c], dkt = X[(C + t) * LD + c];
+      dG[i] = dkt * Kt[t * LD + c] + dqt * Qt[t * LD + c] - dKh[t * LD + c] * Kh[t * LD + c];
+      run = fmaf(dU[t * LD + c], KhC[t * LD + c], run);
+    }
+    if (hf == 0) {
+      float E = 1.0f, Ei = 1.0f;
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        E *= egl[i];
+        Ei *= 1.0f / egl[i];
+      }
+      xs[c] = E;
+      xs[D + c] = Ei;
+      xs[2 * D + c] = run;
+    } else {
+      float P = 1.0f, acc = 0.0f;
+#pragma unroll
+      for (int i = CH - 1; i >= 0; --i) {
+        P *= egl[i];
+        acc += dG[i];
+      }
+      xs[3 * D + c] = P;
+      xs[4 * D + c] = acc;
+    }
+  }
+  __syncthreads();
+  {
+    float E = hf ? xs[c] : 1.0f, Ei = hf ? xs[D + c] : 1.0f, run = hf ? xs[2 * D + c] : 0.0f;
+    float P = hf ? 1.0f : xs[3 * D + c], acc = hf ? 0.0f : xs[4 * D + c];
+    float sfx[CH];  // e^{G_C - G_t}
+#pragma unroll
+    for (int i = CH - 1; i >= 0; --i) {
+      sfx[i] = P;
+      P *= egl[i];
+    }
+    float qr[CH], kr[CH];
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      const int t = tb + i;
+      const int64_t o = ((row0 + t) * a.H + h) * D + c;
+      qr[i] = t < nvalid ? to_f32(((const Tin*)a.q)[o]) : 0.0f;
+      kr[i] = t < nvalid ? to_f32(((const Tin*)a.k)[o]) : 0.0f;
+    }
+    float pre[CH];
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      const int t = tb + i;
+      E *= egl[i];
+      Ei *= 1.0f / egl[i];
       const float dqt = X[t * LD + c], dkt = X[(C + t) * LD + c];
       const float dkh = dKh[t * LD + c], dkhc = dU[t * LD + c];
-      dG[t] = dkt * Kt[t * LD + c] + dqt * Qt[t * LD + c] - dkh * Kh[t * LD + c];
-      pre[t] = run;  // sum_{u < t} dKhC_u KhC_u
+      pre[i] = run;  // sum_{u < t} dKhC_u KhC_u
       run = fmaf(dkhc, KhC[t * LD + c], run);
       if (t < nvalid) {
         const int64_t o = ((row0 + t) * a.H + h) * D + c;
-        a.dq[o] = fmaf(dpd[t], kr[t], dqt * E);
-        a.dk[o] = fmaf(dpd[t], qr[t], dkt * E + dkh * Ei + dkhc * sfx[t]);
+        a.dq[o] = fmaf(dpd[t], kr[i], dqt * E);
+        a.dk[o] = fmaf(dpd[t], qr[i], dkt * E + dkh * Ei + dkhc * sfx[i]);
       }
     }
     const float dec_ec = dec[c] * ec[c];
-    float acc = 0.0f;
 #pragma unroll
-    for (int t = C - 1; t >= 0; --t) {
-      acc += dG[t];
+    for (int i = CH - 1; i >= 0; --i) {
+      const int t = tb + i;
+      acc += dG[i];
       if (t < nvalid)
-        a.dtheta[((row0 + t) * a.H + h) * D + c] = (acc + pre[t] + dec_ec) * dgt[t * LD + c];
+        a.dtheta[((row0 + t) * a.H + h) * D + c] = (acc + pre[i] + dec_ec) * dgt[t * LD + c];
     }
-  } else if (tid - D < nvalid) {
-    a.dbeta[(row0 + tid - D) * a.H + h] = dbt[tid - D];
   }
+  if (tid < nvalid) a.dbeta[(row0 + tid) * a.H + h] = dbt[tid];
 }
 
 template <typename Tin>
@@ -852,7 +1000,7 @@ int launch_bwd_t(const BwdDev& d, int64_t chains, cudaStream_t stream) {
 
 size_t bwd_workspace_size(int B, int H, int T) {
   const size_t nch = ((size_t)T + C - 1) / C;
-  return (size_t)B * H * nch * (2 * kStateF + (size_t)C * D) * sizeof(float);
+  return (size_t)B * H * nch * (2 * kStateF + (size_t)3 * C * D) * sizeof(float);
 }
 
 // (dk = dv = 128 is checked by the caller)
@@ -881,6 +1029,7 @@ int launch_bwd(const BwdParams& p, cudaStream_t stream) {
   d.ws_S = (float*)p.workspace;
   d.ws_dS = d.ws_S + (size_t)chains * nch * kStateF;
   d.ws_dU = d.ws_dS + (size_t)chains * nch * kStateF;
+  d.ws_RU = d.ws_dU + (size_t)chains * nch * C * D;
   d.H = p.H;
   d.T = p.T;
   d.nch = nch;
