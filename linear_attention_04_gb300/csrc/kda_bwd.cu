@@ -390,6 +390,10 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// Waits until at most one of this thread's committed copy groups is pending.
+__device__ __forceinline__ void cp_async_wait_one_pending() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
 
 // Rows row0 .. row0 + 15 of head h of a [tokens, H, D] tensor into a dense
 // [16][D] shared tile with cp.async (rows past nvalid zero-filled).
@@ -403,23 +407,6 @@ __device__ __forceinline__ void stage_rows(const T* g, T* s, const BwdDev& a, in
     const int t = u / kUnits, o = (u % kUnits) * kElems;
     const bool ok = t < nvalid;
     cp_async16(s + t * D + o, (ok ? g0 + (int64_t)t * a.H * D : g0) + o, ok);
-  }
-}
-
-// 16 x 128 fp32 rows of d_out (zero past the sequence end).
-__device__ __forceinline__ void load_dout(const BwdDev& a, int64_t row0, int h, int nvalid,
-                                          float* dO) {
-  constexpr int kPer = C * D / kThreads;
-  float r[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = threadIdx.x + i * kThreads, t = e >> 7, c = e & (D - 1);
-    r[i] = t < nvalid ? a.d_out[((row0 + t) * a.H + h) * D + c] : 0.0f;
-  }
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = threadIdx.x + i * kThreads, t = e >> 7, c = e & (D - 1);
-    dO[t * LD + c] = r[i];
   }
 }
 
@@ -743,50 +730,40 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
   const float* dUg = a.ws_dU + cidx * C * D;
   const float* RUg = a.ws_RU + cidx * 2 * C * D;
 
-  // ---- operands of the chunk, S, dO and dU
+  // Asynchronous copies straight into shared memory, in two groups: the
+  // chunk's d_out rows, dU, R and U (first needed after the inverse), and,
+  // once the chunk's inputs are loaded, S (first needed by [dO; -dR] S^T,
+  // after every product that does not involve it).
+  {
+    const float* dO0 = a.d_out + (row0 * a.H + h) * D;
+    for (int u = tid; u < C * D / 4; u += kThreads) {
+      const int t = u >> 5, c = (u & 31) * 4;
+      const bool ok = t < nvalid;  // d_out rows past the sequence end read as zero
+      cp_async16(X + t * LD + c, dO0 + (ok ? (int64_t)t * a.H * D : 0) + c, ok);
+      cp_async16(dU + t * LD + c, dUg + t * D + c, true);
+    }
+    for (int u = tid; u < 2 * C * D / 4; u += kThreads) {
+      const int r = u >> 5, c = (u & 31) * 4;  // rows 0..15 R (into the V tile), 16..31 U
+      cp_async16((r < C ? V : U) + (r & (C - 1)) * LD + c, RUg + r * D + c, true);
+    }
+    cp_async_commit();
+  }
+  // ---- the chunk's inputs: gate, decay factors and decayed operands
   {
     const int64_t g0 = (row0 * a.H + h) * D;
     load_chunk<Tin>((const Tin*)a.theta + g0, (const Tin*)a.k + g0, (const Tin*)a.q + g0,
                     (const Tin*)a.v + g0, (int64_t)a.H * D, load_beta<Tin>(a, row0, h, nvalid),
                     a.g_min, a.log_decay, nvalid, Qt, Kt, 1.0f, Kh, KhC, EGt, dgt, ec, bt, nullptr);
   }
-  load_dout(a, row0, h, nvalid, X);
-  {
-    float4 u[2], ru[4], x[16];
+  // S (the second copy group), issued after the chunk's own loads
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int e = tid + i * kThreads;
-      u[i] = *(const float4*)(dUg + (e >> 5) * D + (e & 31) * 4);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = tid + i * kThreads;
-      ru[i] = *(const float4*)(RUg + (e >> 5) * D + (e & 31) * 4);
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int e = tid + i * kThreads;
-      x[i] = *(const float4*)(Sg + (size_t)(e >> 5) * D + (e & 31) * 4);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int e = tid + i * kThreads;
-      *(float4*)(dU + (e >> 5) * LD + (e & 31) * 4) = u[i];
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      // R into the V tile, U into the U tile
-      const int e = tid + i * kThreads;
-      *(float4*)((i < 2 ? V : U) + ((e >> 5) & (C - 1)) * LD + (e & 31) * 4) = ru[i];
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int e = tid + i * kThreads;
-      *(float4*)(S + (e >> 5) * LD + (e & 31) * 4) = x[i];
-    }
+  for (int i = 0; i < 16; ++i) {
+    const int e = tid + i * kThreads;
+    cp_async16(S + (e >> 5) * LD + (e & 31) * 4, Sg + (size_t)(e >> 5) * D + (e & 31) * 4, true);
   }
-  // this thread's tile of dS', loaded now so that its latency overlaps the
-  // products that need only S
+  cp_async_commit();
+  // this thread's tile of dS' (registers), loaded now so that its latency
+  // overlaps the products before its first use
   float d[8][8];
   state_load(d, dSg);
   __syncthreads();
@@ -797,7 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
   }
   __syncthreads();
   wy_inverse(Ab, bt, M, Tb, TbT, part);  // (the partial sums' tiles are free here)
-  __syncthreads();
+  cp_async_wait_one_pending();
+  __syncthreads();  // d_out, dU, R and U have arrived
   small16<false>(TbT, dU, X + TILE_F, -1.0f);  // -dR = -Tb^T dU
   __syncthreads();
   {
@@ -812,6 +790,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
     dPiT[nn * LS + m] = nn < m ? p : 0.0f;
     if (nn == m) dpd[m] = p;
   }
+  cp_async_wait_all();
+  __syncthreads();  // S has arrived
   part32_nk(X, S, part);  // [dO; -dR] S^T
   __syncthreads();
   {
