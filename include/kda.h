@@ -95,6 +95,7 @@ extern "C" {
 #define KDA_PATH_TC 2       /* tcgen05/TMEM path, state stepped per 32 tokens (bf16, 128)   */
 #define KDA_PATH_MMA 3      /* register-resident mma.sync path, 16-token steps (bf16, 128)  */
 #define KDA_PATH_TC_SPLIT 4 /* KDA_PATH_TC with the state's bf16 copy as a high/low pair    */
+#define KDA_PATH_MMA_TC 5   /* KDA_PATH_MMA with the intra-chunk A, P on tcgen05 (TMEM)     */
 
 /* gate parameterisation (kda_fwd_args.gate) */
 #define KDA_GATE_SIGMOID 0   /* g = g_min * sigmoid(theta): the bounded gate (default)     */

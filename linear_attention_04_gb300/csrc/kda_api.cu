@@ -59,7 +59,7 @@ int validate(const kda_fwd_args* a) {
   if (a->out_dtype != KDA_DTYPE_BF16 && a->out_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
   if (a->dtype == KDA_DTYPE_F32 && a->out_dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
   if (a->path != KDA_PATH_AUTO && a->path != KDA_PATH_SIMT && a->path != KDA_PATH_TC &&
-      a->path != KDA_PATH_MMA && a->path != KDA_PATH_TC_SPLIT)
+      a->path != KDA_PATH_MMA && a->path != KDA_PATH_TC_SPLIT && a->path != KDA_PATH_MMA_TC)
     return KDA_ERR_INVALID_ARG;
   if (!shape_ok(a->dk) || !shape_ok(a->dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
   // sizes must fit the 32-bit grid and 64-bit offsets used by the kernels
@@ -91,7 +91,7 @@ KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* a, cudaStream_t stream) {
   if (path == KDA_PATH_AUTO) path = kda_select_path(a->dtype, a->dk, a->dv);
   if ((path == KDA_PATH_TC || path == KDA_PATH_TC_SPLIT) && !kda::tc32_supported(a->dtype, a->dk, a->dv))
     return KDA_ERR_UNSUPPORTED_SHAPE;
-  if (path == KDA_PATH_MMA && !kda::mma_supported(a->dtype, a->dk, a->dv))
+  if ((path == KDA_PATH_MMA || path == KDA_PATH_MMA_TC) && !kda::mma_supported(a->dtype, a->dk, a->dv))
     return KDA_ERR_UNSUPPORTED_SHAPE;
   rc = kda::check_device();
   if (rc != KDA_OK) return rc;
@@ -129,7 +129,8 @@ KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* a, cudaStream_t stream) {
   }
   if (path == KDA_PATH_TC || path == KDA_PATH_TC_SPLIT)
     return kda::launch_tc32_jobs(p, nullptr, 0, stream, 0, path == KDA_PATH_TC_SPLIT);
-  if (path == KDA_PATH_MMA) return kda::launch_mma(p, stream);
+  if (path == KDA_PATH_MMA || path == KDA_PATH_MMA_TC)
+    return kda::launch_mma(p, stream, path == KDA_PATH_MMA_TC);
   return kda::launch_simt(p, stream);
 }
 
@@ -318,7 +319,9 @@ KDA_API int kda_selftest_withheld_handoff(const kda_fwd_args* a, long long wait_
   p.gate = a->gate;
   // the job table lives in device memory the copy above fills, in stream order
   const kda::SegJob* jobs = (const kda::SegJob*)workspace;
-  if (a->path == KDA_PATH_MMA) return kda::launch_mma_jobs(p, jobs, 1, stream, (uint64_t)wait_limit_ns);
+  if (a->path == KDA_PATH_MMA || a->path == KDA_PATH_MMA_TC)
+    return kda::launch_mma_jobs(p, jobs, 1, stream, (uint64_t)wait_limit_ns,
+                                a->path == KDA_PATH_MMA_TC);
   return kda::launch_tc32_jobs(p, jobs, 1, stream, (uint64_t)wait_limit_ns, a->path == KDA_PATH_TC_SPLIT);
 }
 

@@ -78,7 +78,9 @@ int launch_bwd(const BwdParams& p, cudaStream_t stream);
 int* status_word_device_ptr();
 
 int launch_simt(const FwdParams& p, cudaStream_t stream);
-int launch_mma(const FwdParams& p, cudaStream_t stream);
+// tc_gram: the intra-chunk products A and P as tcgen05.mma into tensor memory
+// (otherwise warp-level mma.sync); everything else is the same kernel.
+int launch_mma(const FwdParams& p, cudaStream_t stream, bool tc_gram = false);
 
 // One CTA of a segmented launch of the register-resident kernel: a token range
 // of one head, with its own initial/final state and options.
@@ -96,7 +98,7 @@ struct SegJob {
 // Launches one CTA per job over the packed token axis (p.T = total tokens);
 // wait_ns = 0 keeps the default limit of the bounded waits.
 int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStream_t stream,
-                    uint64_t wait_ns = 0);
+                    uint64_t wait_ns = 0, bool tc_gram = false);
 
 // tcgen05/TMEM path with 32-token state steps (kda_tc32.cu): one CTA per job
 // (jobs != null) or per (sequence, head) chain.  `split_s` keeps the state's

@@ -81,7 +81,6 @@ constexpr int kThreads = 32 * (kStateWarps + kIntraWarps);
 // launch allocation).  The split must fit the launch allocation; the host
 // checks it against the compiled register count before the first launch.
 constexpr int kStateRegs = 0, kIntraRegs = 0;
-constexpr int NSLOT = 6;  // chunk slots between the intra and the state warps
 constexpr uint64_t kWaitNs = 2000000000ull;  // default limit of every wait: 2 s
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -101,22 +100,41 @@ constexpr uint32_t SL_EGC = SL_PL + 512;      // [128] fp32 e^{G_C}
 constexpr uint32_t SL_DC = SL_EGC + 512;      // [16] fp32 q_t . k_t
 constexpr uint32_t SLOT_BYTES = SL_DC + 128;
 
-constexpr uint32_t SM_RING = 0;                               // kIntraWarps x STAGE
-constexpr uint32_t SM_KH = SM_RING + kIntraWarps * STAGE;     // kIntraWarps x [16][128] bf16 Kh
-constexpr uint32_t SM_AB = SM_KH + kIntraWarps * TILE;        // kIntraWarps x [16][16] fp32 A
-constexpr uint32_t AB_BYTES = C * C * 4;
-constexpr uint32_t SM_SLOTS = SM_AB + kIntraWarps * AB_BYTES;
-constexpr uint32_t SM_BARS = SM_SLOTS + NSLOT * SLOT_BYTES;
-constexpr int B_FULL = 0;                     // [kIntraWarps] TMA -> intra warp
-constexpr int B_READY = kIntraWarps;          // [NSLOT] intra warp -> state warps
-constexpr int B_FREE = kIntraWarps + NSLOT;   // [NSLOT] state warps (4 arrivals) -> intra warp
-constexpr int NBARS = kIntraWarps + 2 * NSLOT;
-constexpr uint32_t SM_MISC = SM_BARS + NBARS * 8;  // abort flag (+4: job flags)
-constexpr uint32_t SM_RANK = SM_MISC + 16;         // chain-order scratch
-constexpr uint32_t SM_TOTAL = SM_RANK + (kMaxRankedSeqsDev + 1) * 4;
-constexpr uint32_t SMEM_BYTES = SM_TOTAL + 128;    // + alignment slack
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(SLOT_BYTES % 128 == 0 && SM_SLOTS % 128 == 0, "slot alignment");
+constexpr uint32_t AB_BYTES = C * C * 4;       // [16][16] fp32 A of one intra warp
+constexpr uint32_t GA_ROWS = 32 * kIntraWarps;  // tcgen05 Gram operand: [Kt; Qt] of each intra warp
+constexpr uint32_t GA_BYTES = GA_ROWS * D * 2;  // 32 KB, 128-byte swizzled, two 64-channel halves
+constexpr uint32_t GA_HALF = GA_ROWS * 128;     // bytes of one 64-channel half
+constexpr uint32_t GB_HALF = C * 128;           // the same for a [16][128] Kh operand
+constexpr int kTmemCols = 16 * kIntraWarps;     // [16 rows of A | 16 rows of P] x 16 columns per warp
+
+// Shared-memory layout.  kTc: the intra products A and P are tcgen05.mma
+// (operands in 128-byte-swizzled tiles, results in tensor memory), which
+// takes a 32 KB operand tile; the chain-order scratch, used only before the
+// main loops, then lies inside that tile.  Otherwise A and P are warp-level
+// mma.sync over the XOR-swizzled tiles.
+template <bool kTc>
+struct Lay {
+  static constexpr int kSlots = 6;                           // chunk slots between the roles
+  static constexpr uint32_t RING = 0;                        // kIntraWarps x STAGE
+  static constexpr uint32_t KH = RING + kIntraWarps * STAGE; // kIntraWarps x [16][128] bf16 Kh
+  static constexpr uint32_t GA = KH + kIntraWarps * TILE;    // [Kt; Qt] operand (kTc only)
+  static constexpr uint32_t AB = GA + (kTc ? GA_BYTES : 0);  // kIntraWarps x [16][16] fp32 A
+  static constexpr uint32_t SLOTS = AB + kIntraWarps * AB_BYTES;
+  static constexpr uint32_t BARS = SLOTS + kSlots * SLOT_BYTES;
+  static constexpr int B_FULL = 0;                           // [kIntraWarps] TMA -> intra warp
+  static constexpr int B_READY = kIntraWarps;                // [kSlots] intra warp -> state warps
+  static constexpr int B_FREE = B_READY + kSlots;            // [kSlots] state warps (4 arrivals)
+  static constexpr int B_GRAM = B_FREE + kSlots;             // [kIntraWarps] Gram product done
+  static constexpr int NBARS = B_GRAM + (kTc ? kIntraWarps : 0);
+  static constexpr uint32_t MISC = BARS + NBARS * 8;         // abort, job flags, tensor memory address
+  static constexpr uint32_t RANK = kTc ? GA : MISC + 16;     // chain-order scratch
+  static constexpr uint32_t TOTAL = kTc ? MISC + 16 : RANK + (kMaxRankedSeqsDev + 1) * 4;
+  static constexpr uint32_t BYTES = TOTAL + (kTc ? 1024 : 128);  // + alignment slack
+  static_assert(BYTES <= 232448, "shared memory budget");
+  static_assert(SLOT_BYTES % 128 == 0 && SLOTS % 128 == 0, "slot alignment");
+  static_assert(KH % 1024 == 0 && GA % 1024 == 0, "swizzled operand tiles on 1024-byte boundaries");
+  static_assert(!kTc || (kMaxRankedSeqsDev + 1) * 4 <= GA_BYTES, "chain-order scratch fits the tile");
+};
 
 // Byte offset of (row, col) in a tile of 256-byte rows (128 bf16 channels)
 // whose 16-byte chunks are XOR-swizzled by row: eight consecutive rows of one
@@ -128,6 +146,16 @@ __device__ __forceinline__ uint32_t sw256(int row, int col) {
 // Same for 16 x 16 bf16 tiles (32-byte rows): chunk XOR (row / 4).
 __device__ __forceinline__ uint32_t sw32(int row, int col) {
   return (uint32_t)(row * 32 + (((col >> 3) ^ (row >> 2)) & 1) * 16 + (col & 7) * 2);
+}
+
+// Byte offset of (row, col) in a tcgen05 operand tile of 128 bf16 channels per
+// row, K-major with the 128-byte swizzle: two 64-channel halves of
+// `half_bytes` each, rows of 128 bytes (8-row atoms of 1024 bytes), the
+// 16-byte pieces of row r XOR-permuted by r mod 8.
+__device__ __forceinline__ uint32_t sw128(int row, int col, uint32_t half_bytes) {
+  const int c = col & 63;
+  return (uint32_t)((col >> 6) * half_bytes + row * 128 + ((((c >> 3) ^ row) & 7) << 4) +
+                    (c & 7) * 2);
 }
 
 // D += A B with mma.sync m16n8k16, bf16 operands, fp32 accumulators (a pure
@@ -331,18 +359,21 @@ __device__ __forceinline__ void fail(volatile int* abort, int* status) {
 // kFallback: compile the position-wise fallback for chunks whose decay is too
 // steep for the dense tile (only a given, unbounded log-decay can produce
 // them; the bounded gate's kernel carries no such code)
-template <bool kOutBf16, bool kFallback>
+template <bool kOutBf16, bool kFallback, bool kTc>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_fwd_mma_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_th,
                        const __grid_constant__ CUtensorMap tm_v, const MmaArgs args) {
+  using Ly = Lay<kTc>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // pointer arithmetic on the shared array itself keeps the shared address
-  // space visible to the compiler (32-bit shared addressing)
-  unsigned char* sm = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
-  uint64_t* bars = (uint64_t*)(sm + SM_BARS);
-  volatile int* abort = (volatile int*)(sm + SM_MISC);
+  // space visible to the compiler (32-bit shared addressing); the swizzled
+  // tcgen05 operand tiles want a 1024-byte aligned base
+  constexpr uint32_t kAlign = kTc ? 1024u : 128u;
+  unsigned char* sm = smem_raw + ((kAlign - (smem_u32(smem_raw) & (kAlign - 1u))) & (kAlign - 1u));
+  uint64_t* bars = (uint64_t*)(sm + Ly::BARS);
+  volatile int* abort = (volatile int*)(sm + Ly::MISC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // fragment coordinates of mma.sync (g: row group, q: column pair) and of
   // ldmatrix.x4 (mi: which 8x8 matrix this lane addresses, rr: its row)
@@ -364,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     init_state = jb.init;
     final_state = jb.final_state;
   } else {
-    ch = chain_for_block(blockIdx.x, args.H, args.N, args.T, args.cu_seqlens, (int*)(sm + SM_RANK));
+    ch = chain_for_block(blockIdx.x, args.H, args.N, args.T, args.cu_seqlens, (int*)(sm + Ly::RANK));
     if (!ch.valid) {
       // malformed packing table: report it and store nothing
       if (tid == 0) atomicExch(args.status, KDA_ERR_BAD_SEQLENS);
@@ -374,30 +405,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // options read back from shared memory where they are used (keeps them out
   // of the register budget of the main loops)
-  volatile int* sflags = (volatile int*)(sm + SM_MISC + 4);
+  volatile int* sflags = (volatile int*)(sm + Ly::MISC + 4);
   const int h = ch.head;
   const int H = args.H;
   const int L = (int)(ch.t1 - ch.t0);
   const int nchunks = (L + C - 1) / C;
 
+  if constexpr (kTc) {
+    // tensor memory for the intra products: 16 columns per intra warp
+    if (warp == kStateWarps) tmem_alloc((uint32_t*)(sm + Ly::MISC + 8), kTmemCols);
+  }
   if (tid == 0) {
-    for (int i = 0; i < NBARS; ++i) mbar_init(&bars[i], (i >= B_FREE) ? kStateWarps : 1);
+    for (int i = 0; i < Ly::NBARS; ++i)
+      mbar_init(&bars[i], (i >= Ly::B_FREE && i < Ly::B_GRAM) ? kStateWarps : 1);
     *abort = 0;
     *sflags = flags;
     fence_mbar_init();
   }
+  if constexpr (kTc) tc_fence_before();
   __syncthreads();
+  if constexpr (kTc) tc_fence_after();
   const uint32_t sbase = smem_u32(sm);
 
   if (warp >= kStateWarps) {
     // ================================================================ intra warps
     if constexpr (kIntraRegs > 0) set_regs<kIntraRegs>();
     const int iw = warp - kStateWarps;
-    unsigned char* st = sm + SM_RING + iw * STAGE;
-    const uint32_t khs = sbase + SM_KH + iw * TILE;
-    unsigned char* kh = sm + SM_KH + iw * TILE;
-    float* ab = (float*)(sm + SM_AB + iw * AB_BYTES);
-    uint64_t* full = &bars[B_FULL + iw];
+    unsigned char* st = sm + Ly::RING + iw * STAGE;
+    const uint32_t khs = sbase + Ly::KH + iw * TILE;
+    unsigned char* kh = sm + Ly::KH + iw * TILE;
+    float* ab = (float*)(sm + Ly::AB + iw * AB_BYTES);
+    uint64_t* full = &bars[Ly::B_FULL + iw];
     const bool zero_v = *sflags & kJobZeroV;
     auto load = [&](int m) {
       mbar_arrive_expect_tx(full, zero_v ? 3 * TILE : STAGE);
@@ -408,6 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!zero_v) tma_load_3d(st + 3 * TILE, &tm_v, 0, h, row, full);
     };
     int issued = 0, consumed = 0;
+    int gram_issued = 0, gram_waited = 0;  // tcgen05 Gram products of this warp
+    uint32_t tmem = 0;
+    if constexpr (kTc) tmem = *(volatile uint32_t*)(sm + Ly::MISC + 8);
     if (lane == 0 && iw < nchunks) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
@@ -424,10 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const f32x2 kOne = f2(1.0f, 1.0f);
     const f32x2 kZero = 0ull;
     for (int n = iw; n < nchunks; n += kIntraWarps) {
-      const int slot = n % NSLOT;
+      const int slot = n % Ly::kSlots;
       const int nvalid = min(C, L - n * C);
-      unsigned char* sl = sm + SM_SLOTS + slot * SLOT_BYTES;
-      const uint32_t sls = sbase + SM_SLOTS + slot * SLOT_BYTES;
+      unsigned char* sl = sm + Ly::SLOTS + slot * SLOT_BYTES;
+      const uint32_t sls = sbase + Ly::SLOTS + slot * SLOT_BYTES;
       // beta of the chunk (lane t holds beta_t), issued before the waits
       float beta_l = 0.0f;
       if (lane < nvalid) beta_l = __bfloat162float(args.beta[(ch.t0 + (int64_t)n * C + lane) * H + h]);
@@ -437,9 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++consumed;
       if (lane == 0) KTRACE(n, 5);
-      if (n >= NSLOT &&
-          !__all_sync(0xffffffffu,
-                      mbar_wait(&bars[B_FREE + slot], ((n / NSLOT) - 1) & 1, abort, args.wait_ns))) {
+      if (n >= Ly::kSlots &&
+          !__all_sync(0xffffffffu, mbar_wait(&bars[Ly::B_FREE + slot], ((n / Ly::kSlots) - 1) & 1,
+                                             abort, args.wait_ns))) {
         bad = true;
         break;
       }
@@ -488,11 +529,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const f32x2 r0 = f2(ex2_approx(-f2lo(G0)), ex2_approx(-f2hi(G0)));
         const f32x2 r1 = f2(ex2_approx(-f2lo(G1)), ex2_approx(-f2hi(G1)));
         const f32x2 kh0 = mul2(k0, r0), kh1 = mul2(k1, r1);
-        *(uint2*)(sl + SL_XB + sw256(t, 4 * lane)) =
-            make_uint2(f2_to_bf2(mul2(k0, e0)), f2_to_bf2(mul2(k1, e1)));
-        *(uint2*)(sl + SL_XB + sw256(16 + t, 4 * lane)) =
-            make_uint2(f2_to_bf2(mul2(q0, e0)), f2_to_bf2(mul2(q1, e1)));
-        *(uint2*)(kh + sw256(t, 4 * lane)) = make_uint2(f2_to_bf2(kh0), f2_to_bf2(kh1));
+        const uint2 ktw = make_uint2(f2_to_bf2(mul2(k0, e0)), f2_to_bf2(mul2(k1, e1)));
+        const uint2 qtw = make_uint2(f2_to_bf2(mul2(q0, e0)), f2_to_bf2(mul2(q1, e1)));
+        const uint2 khw = make_uint2(f2_to_bf2(kh0), f2_to_bf2(kh1));
+        *(uint2*)(sl + SL_XB + sw256(t, 4 * lane)) = ktw;
+        *(uint2*)(sl + SL_XB + sw256(16 + t, 4 * lane)) = qtw;
+        if constexpr (kTc) {
+          // the tensor-core operands: [Kt; Qt] in this warp's 32 rows of the
+          // shared A tile, Kh as this warp's B tile
+          *(uint2*)(sm + Ly::GA + sw128(32 * iw + t, 4 * lane, GA_HALF)) = ktw;
+          *(uint2*)(sm + Ly::GA + sw128(32 * iw + 16 + t, 4 * lane, GA_HALF)) = qtw;
+          *(uint2*)(kh + sw128(t, 4 * lane, GB_HALF)) = khw;
+        } else {
+          *(uint2*)(kh + sw256(t, 4 * lane)) = khw;
+        }
         khr[t][0] = kh0;
         khr[t][1] = kh1;
         const f32x2 qk = fma2(q1, k1, mul2(q0, k0));
@@ -506,6 +556,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < C; ++t)
           *(uint2*)(sl + SL_KC + sw256(t, 4 * lane)) =
               make_uint2(f2_to_bf2(mul2(khr[t][0], c0)), f2_to_bf2(mul2(khr[t][1], c1)));
+      }
+      if constexpr (kTc) {
+        // the Gram product A, P starts now and overlaps the work below
+        fence_proxy_async_smem();  // the operand writes above, for the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t ga = sbase + Ly::GA, gb = khs;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + 16 * iw, sdesc_sw128(ga + (kk >> 2) * GA_HALF + (kk & 3) * 32),
+                   sdesc_sw128(gb + (kk >> 2) * GB_HALF + (kk & 3) * 32), idesc_bf16_f32(128, C),
+                   kk > 0);
+          mma_commit(&bars[Ly::B_GRAM + iw]);
+        }
+        ++gram_issued;
       }
       // V into the slot (swizzled)
 #pragma unroll
@@ -559,7 +625,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       refill();
       // ---- phase B: A = Kt Kh^T and P = Qt Kh^T (M = N = 16, K = 128)
-      if (!fallback) {
+      if constexpr (kTc) {
+        // One M = 128 tcgen05.mma per 16 channels of K, issued by lane 0 after
+        // phase A: rows 32 iw .. 32 iw + 31 of the shared A tile are this
+        // warp's [Kt; Qt] (the other rows belong to the other intra warps and
+        // land in tensor memory lanes this warp never reads), B is this warp's
+        // Kh, and the 16 result columns are this warp's own.  Waited for in
+        // every chunk (the next chunk's operands overwrite the tiles it
+        // reads); a position-wise chunk ignores its result.
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[Ly::B_GRAM + iw], (gram_issued - 1) & 1, abort,
+                                               args.wait_ns))) {
+          bad = true;
+          break;
+        }
+        ++gram_waited;
+        tc_fence_after();
+        if (!fallback) {
+        // lane l reads row 32 iw + l of the result: row l of A (l < 16) or row
+        // l - 16 of P, 16 columns
+        uint32_t dr[C];
+        tmem_ld_x16(tmem + ((uint32_t)(32 * iw) << 16) + 16 * iw, dr);
+        tmem_wait_ld();
+        if (lane < C) {
+          // strictly lower, scaled by beta of the row's token
+          const int r = lane;
+#pragma unroll
+          for (int s4 = 0; s4 < C; s4 += 4)
+            *(float4*)(ab + r * C + s4) = make_float4(
+                s4 < r ? beta_l * __uint_as_float(dr[s4]) : 0.0f,
+                s4 + 1 < r ? beta_l * __uint_as_float(dr[s4 + 1]) : 0.0f,
+                s4 + 2 < r ? beta_l * __uint_as_float(dr[s4 + 2]) : 0.0f,
+                s4 + 3 < r ? beta_l * __uint_as_float(dr[s4 + 3]) : 0.0f);
+        } else {
+          // strictly lower P as a bf16 high/low pair
+          const int r = lane - C;
+          uint32_t hw[C / 2], lw[C / 2];
+#pragma unroll
+          for (int s2 = 0; s2 < C; s2 += 2) {
+            const float p0 = s2 < r ? __uint_as_float(dr[s2]) : 0.0f;
+            const float p1 = s2 + 1 < r ? __uint_as_float(dr[s2 + 1]) : 0.0f;
+            const uint32_t hi = pack_bf16x2(p0, p1);
+            const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&hi);
+            hw[s2 / 2] = hi;
+            lw[s2 / 2] = pack_bf16x2(p0 - __low2float(hb), p1 - __high2float(hb));
+          }
+          *(uint4*)(sl + SL_P + sw32(r, 0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *(uint4*)(sl + SL_P + sw32(r, 8)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+          *(uint4*)(sl + SL_PL + sw32(r, 0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          *(uint4*)(sl + SL_PL + sw32(r, 8)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+        }
+        // the tensor-memory read is complete before this warp's next product
+        tc_fence_before();
+        }
+      } else if (!fallback) {
       float accA[2][4], accP[2][4];
 #pragma unroll
       for (int j = 0; j < 2; ++j)
@@ -604,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               pack_bf16x2(p2 - __low2float(b23), p3 - __high2float(b23));
         }
       }
-      }  // dense phase B
+      }  // mma.sync phase B
       __syncwarp();
       if (lane == 0) KTRACE(n, 8);
       if (lane < C) {
@@ -661,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (a test job can withhold its first hand-off: the state warps' bounded
       // wait then runs out and reports KDA_ERR_DEVICE_TIMEOUT)
       if (lane == 0 && !(n == 0 && (*sflags & kJobTestWithholdFirst))) {
-        mbar_arrive(&bars[B_READY + slot]);
+        mbar_arrive(&bars[Ly::B_READY + slot]);
         KTRACE(n, 10);
       }
     }
@@ -669,6 +787,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a refill issued for a chunk this warp never waited for is drained
     // before the CTA releases its shared memory
     if (lane == 0 && issued > consumed) mbar_wait_drain(full, consumed & 1, args.wait_ns);
+    if constexpr (kTc) {
+      // every product of this warp has completed before the tensor memory is
+      // released (a bounded wait, as everywhere)
+      if (gram_issued > gram_waited)
+        mbar_wait_drain(&bars[Ly::B_GRAM + iw], (gram_issued - 1) & 1, args.wait_ns);
+      __syncwarp();
+      tc_fence_before();
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kIntraWarps) : "memory");  // the four intra warps
+      tc_fence_after();
+      if (iw == 0) tmem_dealloc(tmem, kTmemCols);
+    }
   } else {
     // ================================================================ state warps
     if constexpr (kStateRegs > 0) set_regs<kStateRegs>();
@@ -689,11 +818,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     bool bad = false;
     for (int n = 0; n < nchunks; ++n) {
-      const int slot = n % NSLOT;
-      const unsigned char* sl = sm + SM_SLOTS + slot * SLOT_BYTES;
-      const uint32_t sls = sbase + SM_SLOTS + slot * SLOT_BYTES;
+      const int slot = n % Ly::kSlots;
+      const unsigned char* sl = sm + Ly::SLOTS + slot * SLOT_BYTES;
+      const uint32_t sls = sbase + Ly::SLOTS + slot * SLOT_BYTES;
       if (!__all_sync(0xffffffffu,
-                      mbar_wait(&bars[B_READY + slot], (n / NSLOT) & 1, abort, args.wait_ns))) {
+                      mbar_wait(&bars[Ly::B_READY + slot], (n / Ly::kSlots) & 1, abort, args.wait_ns))) {
         bad = true;
         break;
       }
@@ -843,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // the slot's reads are all consumed (their values fed the products above)
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_FREE + slot]);
+      if (lane == 0) mbar_arrive(&bars[Ly::B_FREE + slot]);
       if (tid == 0) KTRACE(n, 4);
     }
     if (bad) fail(abort, args.status);
@@ -872,7 +1001,7 @@ bool mma_supported(int dtype, int dk, int dv) {
 }
 
 int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStream_t stream,
-                    uint64_t wait_ns) {
+                    uint64_t wait_ns, bool tc_gram) {
   if (!mma_supported(p.dtype, p.dk, p.dv)) return KDA_ERR_UNSUPPORTED_SHAPE;
   const int64_t tokens = p.cu_seqlens ? (int64_t)p.T : (int64_t)p.N * p.T;
   if (tokens <= 0) {
@@ -891,10 +1020,19 @@ int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStrea
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxAttrDevices) return KDA_ERR_CUDA;
   std::call_once(g_attr_once[dev], [dev]() {
     cudaError_t err = cudaSuccess;
-    for (const void* fn : {(const void*)kda_fwd_mma_kernel<false, false>, (const void*)kda_fwd_mma_kernel<true, false>,
-                           (const void*)kda_fwd_mma_kernel<false, true>, (const void*)kda_fwd_mma_kernel<true, true>}) {
+    const void* fns[8] = {(const void*)kda_fwd_mma_kernel<false, false, false>,
+                          (const void*)kda_fwd_mma_kernel<true, false, false>,
+                          (const void*)kda_fwd_mma_kernel<false, true, false>,
+                          (const void*)kda_fwd_mma_kernel<true, true, false>,
+                          (const void*)kda_fwd_mma_kernel<false, false, true>,
+                          (const void*)kda_fwd_mma_kernel<true, false, true>,
+                          (const void*)kda_fwd_mma_kernel<false, true, true>,
+                          (const void*)kda_fwd_mma_kernel<true, true, true>};
+    for (int f = 0; f < 8; ++f) {
+      const void* fn = fns[f];
+      const int bytes = (int)(f < 4 ? Lay<false>::BYTES : Lay<true>::BYTES);
       if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
       if (kStateRegs > 0 && err == cudaSuccess) {
         // setmaxnreg.inc can only draw on the registers the block was launched
         // with: a split above the compiled launch allocation would wait forever
@@ -927,18 +1065,33 @@ int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStrea
   const unsigned grid = jobs ? (unsigned)njobs : (unsigned)(p.N * p.H);
   if (grid == 0) return KDA_OK;
   const bool fb = p.gate == KDA_GATE_LOG_DECAY;
-  if (a.out_bf16 && fb)
-    kda_fwd_mma_kernel<true, true><<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
-  else if (a.out_bf16)
-    kda_fwd_mma_kernel<true, false><<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
-  else if (fb)
-    kda_fwd_mma_kernel<false, true><<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
-  else
-    kda_fwd_mma_kernel<false, false><<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mth, mv, a);
+  if (tc_gram) {
+    constexpr uint32_t sm = Lay<true>::BYTES;
+    if (a.out_bf16 && fb)
+      kda_fwd_mma_kernel<true, true, true><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
+    else if (a.out_bf16)
+      kda_fwd_mma_kernel<true, false, true><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
+    else if (fb)
+      kda_fwd_mma_kernel<false, true, true><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
+    else
+      kda_fwd_mma_kernel<false, false, true><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
+  } else {
+    constexpr uint32_t sm = Lay<false>::BYTES;
+    if (a.out_bf16 && fb)
+      kda_fwd_mma_kernel<true, true, false><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
+    else if (a.out_bf16)
+      kda_fwd_mma_kernel<true, false, false><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
+    else if (fb)
+      kda_fwd_mma_kernel<false, true, false><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
+    else
+      kda_fwd_mma_kernel<false, false, false><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
+  }
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
-int launch_mma(const FwdParams& p, cudaStream_t stream) { return launch_mma_jobs(p, nullptr, 0, stream); }
+int launch_mma(const FwdParams& p, cudaStream_t stream, bool tc_gram) {
+  return launch_mma_jobs(p, nullptr, 0, stream, 0, tc_gram);
+}
 
 }  // namespace kda
 

@@ -27,7 +27,7 @@ KDA_ERR_UNSUPPORTED_SHAPE = -7
 KDA_ERR_SCRATCH_TOO_SMALL = -8
 KDA_ERR_BAD_SEQLENS = -9
 
-PATHS = {"auto": 0, "simt": 1, "tc": 2, "mma": 3, "tc_split": 4}
+PATHS = {"auto": 0, "simt": 1, "tc": 2, "mma": 3, "tc_split": 4, "mma_tc": 5}
 GATES = {"sigmoid": 0, "log_decay": 1}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 

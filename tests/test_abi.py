@@ -64,6 +64,7 @@ def _args(**over):
     (dict(out_dtype=3), binding.KDA_ERR_INVALID_ARG),
     (dict(dtype=1, out_dtype=0), binding.KDA_ERR_INVALID_ARG),
     (dict(path=9), binding.KDA_ERR_INVALID_ARG),
+    (dict(path=6), binding.KDA_ERR_INVALID_ARG),
     (dict(dk=24), binding.KDA_ERR_UNSUPPORTED_SHAPE),
     (dict(dv=256), binding.KDA_ERR_UNSUPPORTED_SHAPE),
     (dict(q=0x1001), binding.KDA_ERR_MISALIGNED),
@@ -180,7 +181,7 @@ def test_gate_mode_host_checks():
     a = _args(gate=1, g_min=0.0)
     assert lib.kda_chunk_fwd_ex(ctypes.byref(a), None) != binding.KDA_ERR_INVALID_ARG
     # every tensor-core path takes both gates; they need bf16 inputs at 128 x 128
-    for path in (2, 3, 4):
+    for path in (2, 3, 4, 5):
         a = _args(gate=1, path=path)
         assert lib.kda_chunk_fwd_ex(ctypes.byref(a), None) not in (
             binding.KDA_ERR_INVALID_ARG, binding.KDA_ERR_UNSUPPORTED_SHAPE)

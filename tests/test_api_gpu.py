@@ -71,7 +71,7 @@ def test_slow_decay_regime(path):
     assert_close(f64(S), rS, TOL[torch.bfloat16], f"slow decay state ({path})")
 
 
-@pytest.mark.parametrize("path", ["simt", "mma", "tc"])
+@pytest.mark.parametrize("path", ["simt", "mma", "mma_tc", "tc"])
 def test_malformed_cu_seqlens_reported_and_the_context_survives(path):
     lens = [40, 24, 32]
     w = Workload("badcu", B=3, H=2, T=0, dk=128, dv=128, dtype=torch.bfloat16, varlen=True)

@@ -17,7 +17,7 @@ from parity import TOL, assert_close, f64, oracle_full
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("path", [binding.PATHS["mma"], binding.PATHS["tc"]])
+@pytest.mark.parametrize("path", [binding.PATHS["mma"], binding.PATHS["mma_tc"], binding.PATHS["tc"]])
 def test_withheld_handoff_reports_a_timeout_and_the_context_survives(path):
     w = Workload("fail", B=1, H=2, T=256, dk=128, dv=128, dtype=torch.bfloat16)
     inp = make_inputs(w, seed=404)

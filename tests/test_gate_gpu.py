@@ -38,8 +38,8 @@ def _run(inp, theta, path, gate):
 
 
 @pytest.mark.parametrize("dtype,path", [(torch.float32, "simt"), (torch.bfloat16, "simt"),
-                                        (torch.bfloat16, "mma"), (torch.bfloat16, "tc"),
-                                        (torch.bfloat16, "tc_split")])
+                                        (torch.bfloat16, "mma"), (torch.bfloat16, "mma_tc"),
+                                        (torch.bfloat16, "tc"), (torch.bfloat16, "tc_split")])
 def test_log_decay_gate_vs_oracle(dtype, path):
     # logits ~ N(2, 1): |g| ~ 2.2 per token, the decay rate of the named
     # workloads (the bf16 operand plan's error grows past the 2e-2 bar once the
@@ -53,7 +53,7 @@ def test_log_decay_gate_vs_oracle(dtype, path):
     assert_close(f64(S), rS, tol, f"log-decay gate state ({path}, {dtype})")
 
 
-@pytest.mark.parametrize("path", ["mma", "tc"])
+@pytest.mark.parametrize("path", ["mma", "mma_tc", "tc"])
 def test_unbounded_softplus_control(path):
     # logits ~ N(8, 1): every 16-token chunk reaches -G ~ 128 > 88.7 with the
     # -softplus gate; the bounded gate on the same logits stays below 80
@@ -81,7 +81,8 @@ def test_unbounded_softplus_control(path):
     assert_close(f64(ob), rb, TOL[torch.bfloat16], "bounded gate, same logits")
 
 
-def test_fallback_on_some_chunks_only():
+@pytest.mark.parametrize("path", ["mma", "mma_tc"])
+def test_fallback_on_some_chunks_only(path):
     """logits ~ N(4.75, 1): some 16-token chunks (about a fifth) pass the dense tile's limit
     (-G = 126 / log2 e = 87.3 on any channel) and some do not, so the
     register-resident path mixes dense and position-wise chunks in one chain."""
@@ -91,6 +92,6 @@ def test_fallback_on_some_chunks_only():
     assert 0.05 < share < 0.99
     ro, rS = oracle.fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(g), f64(inp["beta"]),
                         -5.0, None, theta_is_g=True)
-    o, S = _run(inp, g, "mma", "log_decay")
+    o, S = _run(inp, g, path, "log_decay")
     assert_close(f64(o), ro, TOL[torch.bfloat16], "mixed fallback out")
     assert_close(f64(S), rS, TOL[torch.bfloat16], "mixed fallback state")

@@ -20,7 +20,7 @@ def _paths(dtype, dk, dv):
         return ["simt"]
     ps = ["simt"]
     if dk == 128 and dv == 128:
-        ps += ["tc", "tc_split", "mma"]
+        ps += ["tc", "tc_split", "mma", "mma_tc"]
     return ps
 
 
