@@ -375,7 +375,7 @@ def run_ours(args, rank, world, local):
     achieved = alg / avg_launch_s / 1e9
     achieved32 = alg32 / avg_launch_s / 1e9
     kernels = {"tc": "kda_fwd_tc32_kernel", "tc_split": "kda_fwd_tc32_kernel",
-               "mma": "kda_fwd_mma_kernel"}
+               "mma": "kda_fwd_mma_kernel", "mma_tc": "kda_fwd_mma_kernel"}
     kname = kernels.get(path, "kda_fwd_simt_kernel")
     if ws is not None:
         kname = kernels.get(seg_kernel, "kda_fwd_tc32_kernel")
@@ -708,7 +708,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="train_bf16")
-    ap.add_argument("--path", choices=["auto", "simt", "tc", "tc_split", "mma"], default="auto")
+    ap.add_argument("--path", choices=["auto", "simt", "tc", "tc_split", "mma", "mma_tc"],
+                    default="auto")
     ap.add_argument("--batch", type=int, default=0,
                     help="replace the workload's B (fixed-length workloads; profiling cases)")
     ap.add_argument("--heads", type=int, default=0,
