@@ -118,14 +118,6 @@ KDA_DEV void tma_load_3d(void* dst_smem, const CUtensorMap* map, int c0, int c1,
       "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
 }
-// Starts bringing a tile of a tensor into L2 (no shared memory, no completion
-// to wait for): a later TMA load of the same box then hits L2.
-KDA_DEV void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   (uint64_t)map),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
 KDA_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
 }

@@ -213,6 +213,13 @@ KDA_DEV f32x2 tf32_rna2(f32x2 v) {
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(b) : "f"(f2hi(v)));
   return (uint64_t)a | ((uint64_t)b << 32);
 }
+KDA_DEV void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   (uint64_t)map),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 template <int N>
 __device__ __forceinline__ void set_regs() {
   if constexpr (N > kLaunchRegs)
