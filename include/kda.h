@@ -59,6 +59,12 @@
  * is queued.  A device-side wait that runs out (the tensor-core paths bound
  * every wait) records KDA_ERR_DEVICE_TIMEOUT in a per-device status word that
  * kda_device_status() reads after the caller has synchronised.
+ *
+ * Threads: every entry point may be called from several host threads at
+ * once.  The only state the library keeps is per device and written once:
+ * the device check, the kernels' shared-memory attributes, the status-word
+ * and scratch-area addresses.  Calls that share an output buffer, a
+ * workspace or the no-alloc scratch area must not overlap.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -178,6 +184,13 @@ typedef struct kda_fwd_args {
 } kda_fwd_args;
 
 KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* args, cudaStream_t stream);
+
+/* Device workspace the fused forward entry points (kda_chunk_fwd, _f32, _ex)
+ * need: always 0 -- every intermediate of the chunked form lives in shared
+ * memory, registers or tensor memory.  Kept so that callers can size a
+ * workspace the same way for every entry point (the segmented forward and
+ * the backward do need one). */
+KDA_API size_t kda_chunk_fwd_workspace_size(int B, int H, int T, int dk, int dv);
 
 /*
  * kda_chunk_fwd_segmented -- the operation of kda_chunk_fwd_ex, cut along the

@@ -84,6 +84,8 @@ KDA_API int kda_select_path(int dtype, int dk, int dv) {
   return kda::mma_supported(dtype, dk, dv) ? KDA_PATH_MMA : KDA_PATH_SIMT;
 }
 
+KDA_API size_t kda_chunk_fwd_workspace_size(int, int, int, int, int) { return 0; }
+
 KDA_API int kda_chunk_fwd_ex(const kda_fwd_args* a, cudaStream_t stream) {
   int rc = kda::validate(a);
   if (rc != KDA_OK) return rc;

@@ -28,6 +28,13 @@ def test_header_declares_entry_points():
         assert n in names
 
 
+def test_fused_forward_needs_no_workspace():
+    lib = binding.load()
+    lib.kda_chunk_fwd_workspace_size.restype = ctypes.c_size_t
+    for shape in ((8, 32, 8192, 128, 128), (1, 2, 64, 16, 16), (3, 1, 0, 64, 128)):
+        assert lib.kda_chunk_fwd_workspace_size(*shape) == 0
+
+
 def test_library_exports_every_declared_symbol():
     lib = binding.load()
     missing = [n for n in _declared_symbols() if not hasattr(lib, n)]
