@@ -176,6 +176,11 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, theta: torc
     (N = B, or the number of sequences when cu_seqlens [N+1] int32 is given
     and B == 1).  Returns (out, final_state or None).  Asynchronous on
     ``stream`` (default: torch's current stream).
+    ``path``: "auto" (the register-resident kernel for bf16 at dk = dv = 128,
+    else the fp32 SIMT kernel), "mma", "mma_tc" (the same with the intra-chunk
+    A and P on tcgen05), "tc" / "tc_split" (the tcgen05 kernel with 32-token
+    state steps, more accurate under slow decay), or "simt".  ``gate``:
+    "sigmoid" (g = g_min sigmoid(theta)) or "log_decay" (theta is g).
     """
     lib = load()
     B, T, H, dk = q.shape
