@@ -27,15 +27,16 @@
 // Two launches over a caller workspace:
 //   1. kda_bwd_recurrences_kernel, two CTAs per chain (independent of each
 //      other): the forward recurrence, writing the state at the start of every
-//      chunk; and the reverse recurrence of dS, writing dS' and dU of every
-//      chunk, and dV;
+//      chunk and R, U of every chunk; and the reverse recurrence of dS, writing
+//      dS' and dU of every chunk, and dV;
 //   2. kda_bwd_grads_kernel, one CTA per chunk, all chunks in parallel: every
-//      other gradient from S, dS', dU and the chunk's inputs.
-// The recurrences carry their 128 x 128 state in registers (an 8 x 8 tile per
-// thread) with a copy in shared memory for the products that contract over
-// it, and stage the next chunk's inputs in shared memory with cp.async while
-// the current chunk computes.  Every product is an fp32 FMA over shared-memory
-// operands.
+//      other gradient from S, dS', dU, R, U and the chunk's inputs.
+// The recurrences carry their 128 x 128 state in registers with a copy in
+// shared memory for the products that contract over it, and stage the next
+// chunk's inputs in shared memory with cp.async while the current chunk
+// computes.  The forward recurrence is warp-specialised: four warps form the
+// next chunk's operands while the other four run the current chunk's state
+// products.  Every product is an fp32 FMA over shared-memory operands.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -517,73 +518,332 @@ __device__ __forceinline__ void state_update(float (&st)[8][8], const float* ec,
 }
 
 // ------------------------------------------------------- forward recurrence
+// Warp-specialised: warps 0..3 (the state group) carry S and run the products
+// that need it; warps 4..7 (the prep group) form the next chunk's operands --
+// gate, decay factors, decayed tiles, Ab and the inverse -- meanwhile, into
+// one of two buffers.  The groups hand buffers over through named barriers
+// (arrive by one group, sync by the other, 256 threads each); each group also
+// has its own 128-thread barrier.
+constexpr int kGroup = kThreads / 2;
+constexpr int BAR_SG = 1, BAR_PG = 2, BAR_READY = 3, BAR_FREE = 5;  // READY/FREE: + buffer
+__device__ __forceinline__ void bar_group(int id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kGroup) : "memory");
+}
+__device__ __forceinline__ void bar_sync_all(int id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kThreads) : "memory");
+}
+__device__ __forceinline__ void bar_arrive_all(int id) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "n"(kThreads) : "memory");
+}
+
+// One chunk's operands on the 128 threads of the prep group, one channel per
+// thread, sequential over the tokens: the same per-element arithmetic as
+// load_chunk (the gradient kernel forms the same factors).
+template <typename Tin>
+__device__ __forceinline__ void prep_chunk(const Tin* th0, const Tin* k0, const Tin* v0,
+                                           float bval, float g_min, int log_decay, int nvalid,
+                                           float* Kt, float* Kh, float* KhC, float* ec, float* bt,
+                                           float* V, int gt) {
+  const int c = gt;
+  float xr[C], kr[C], vr[C], egr[C];
+#pragma unroll
+  for (int t = 0; t < C; ++t) {
+    const bool ok = t < nvalid;
+    xr[t] = ok ? to_f32(th0[t * D + c]) : 0.0f;
+    kr[t] = ok ? to_f32(k0[t * D + c]) : 0.0f;
+    vr[t] = ok ? to_f32(v0[t * D + c]) : 0.0f;
+  }
+  float E = 1.0f, Ei = 1.0f;
+#pragma unroll
+  for (int t = 0; t < C; ++t) {
+    float g = 0.0f;
+    if (t < nvalid) {
+      if (log_decay) {
+        g = xr[t];
+      } else {
+        const float x = xr[t];
+        const float e = expf(-fabsf(x));
+        const float big = 1.0f / (1.0f + e), small = e * big;
+        g = g_min * (x >= 0.0f ? big : small);
+      }
+    }
+    const float eg = expf(g);
+    E *= eg;
+    Ei *= 1.0f / eg;
+    egr[t] = eg;
+    Kt[t * LD + c] = kr[t] * E;
+    Kh[t * LD + c] = kr[t] * Ei;
+    V[t * LD + c] = vr[t];
+  }
+  ec[c] = E;
+  float P = 1.0f;
+#pragma unroll
+  for (int t = C - 1; t >= 0; --t) {
+    KhC[t * LD + c] = kr[t] * P;
+    P *= egr[t];
+  }
+  if (gt < C) bt[gt] = bval;
+}
+
+// (I + Diag(b) Ab)^{-1} as in wy_inverse, on the 128 threads of one group
+// (two entries per thread: rows i and i + 8 of column j), with that group's
+// barrier between the rounds.  M and Tb are complete after the group's next
+// barrier.
+__device__ __forceinline__ void wy_inverse_group(const float* Ab, const float* bt, float* M,
+                                                 float* Tb, float* scratch, int gt, int bar) {
+  const int i0 = gt >> 4, j = gt & 15;
+  float* B0 = scratch;
+  float* B1 = B0 + SM16_F;
+  float* B2 = B1 + SM16_F;
+  float* B3 = B2 + SM16_F;
+  float* B4 = B3 + SM16_F;
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const int i = i0 + 8 * h2, ij = i * LS + j;
+    const float n = j < i ? bt[i] * Ab[ij] : 0.0f;
+    B0[ij] = n;
+    B1[ij] = (i == j ? 1.0f : 0.0f) - n;
+  }
+  bar_group(bar);
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const int i = i0 + 8 * h2;
+    float x = 0.0f;
+#pragma unroll
+    for (int l = 0; l < C; ++l) x = fmaf(B0[i * LS + l], B0[l * LS + j], x);
+    B2[i * LS + j] = x;
+  }
+  bar_group(bar);
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const int i = i0 + 8 * h2, ij = i * LS + j;
+    float q = B1[ij], x = 0.0f;
+#pragma unroll
+    for (int l = 0; l < C; ++l) {
+      q = fmaf(B1[i * LS + l], B2[l * LS + j], q);
+      x = fmaf(B2[i * LS + l], B2[l * LS + j], x);
+    }
+    B3[ij] = q;
+    B4[ij] = x;
+  }
+  bar_group(bar);
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const int i = i0 + 8 * h2, ij = i * LS + j;
+    float q = B3[ij], x = 0.0f;
+#pragma unroll
+    for (int l = 0; l < C; ++l) {
+      q = fmaf(B3[i * LS + l], B4[l * LS + j], q);
+      x = fmaf(B4[i * LS + l], B4[l * LS + j], x);
+    }
+    B1[ij] = q;
+    B0[ij] = x;
+  }
+  bar_group(bar);
+  const float bj = bt[j];
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const int i = i0 + 8 * h2, ij = i * LS + j;
+    float q = B1[ij];
+#pragma unroll
+    for (int l = 0; l < C; ++l) q = fmaf(B1[i * LS + l], B0[l * LS + j], q);
+    M[ij] = q;
+    Tb[ij] = q * bj;
+  }
+}
+
+// The state group's register tile of the 128 x 128 state: element [i][c] of
+// st is row 8 ig + i, column 32 (c / 4) + 4 jg + c % 4 (ig = gt / 8, jg = gt % 8).
+__device__ __forceinline__ void group_state_store(const float (&st)[8][16], float* dst, int ld,
+                                                  int gt) {
+  const int ig = gt >> 3, jg = gt & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      *(float4*)(dst + (size_t)(8 * ig + i) * ld + 32 * g + 4 * jg) =
+          make_float4(st[i][4 * g], st[i][4 * g + 1], st[i][4 * g + 2], st[i][4 * g + 3]);
+}
+__device__ __forceinline__ void group_state_load(float (&st)[8][16], const float* src, int gt) {
+  const int ig = gt >> 3, jg = gt & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const float4 x = src ? *(const float4*)(src + (size_t)(8 * ig + i) * D + 32 * g + 4 * jg)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      st[i][4 * g] = x.x;
+      st[i][4 * g + 1] = x.y;
+      st[i][4 * g + 2] = x.z;
+      st[i][4 * g + 3] = x.w;
+    }
+}
+// Rows row0 .. row0 + 15 of head h of a [tokens, H, D] tensor into a dense
+// [16][D] shared tile with cp.async, issued by the 128 threads of one group.
+template <typename T>
+__device__ __forceinline__ void stage_rows_group(const T* g, T* s, const BwdDev& a, int64_t row0,
+                                                 int h, int nvalid, int gt) {
+  constexpr int kUnits = (int)(D * sizeof(T) / 16);
+  constexpr int kElems = (int)(16 / sizeof(T));
+  const T* g0 = g + (row0 * a.H + h) * D;
+  for (int u = gt; u < C * kUnits; u += kGroup) {
+    const int t = u / kUnits, o = (u % kUnits) * kElems;
+    const bool ok = t < nvalid;
+    cp_async16(s + t * D + o, (ok ? g0 + (int64_t)t * a.H * D : g0) + o, ok);
+  }
+}
+
+constexpr int BUF_F = 3 * TILE_F + SM16_F + D + C;  // one prep buffer: Kt, KhC, V/R, Tb, e^{G_C}, beta
+static_assert(BUF_F % 4 == 0, "prep buffers on 16-byte boundaries");
+
 template <typename Tin>
 __device__ __forceinline__ void states_chain(const BwdDev& a, int64_t chain) {
   extern __shared__ __align__(16) float smf[];
-  float* S = smf;
-  float* Kt = S + STATE_F;
-  float* Kh = Kt + TILE_F;
-  float* KhC = Kh + TILE_F;
-  float* V = KhC + TILE_F;  // V, then R
-  float* U = V + TILE_F;
-  float* part = U + TILE_F;  // 4 tiles
-  float* Ab = part + 4 * TILE_F;
+  float* S = smf;                       // the state group's copy of S for Kt S
+  float* buf = S + STATE_F;             // two prep buffers
+  float* Kh = buf + 2 * BUF_F;          // prep group: Kh, Ab, M, inverse scratch
+  float* Ab = Kh + TILE_F;
   float* M = Ab + SM16_F;
-  float* Tb = M + SM16_F;
-  float* ec = Tb + SM16_F;
-  float* bt = ec + D;
-  Tin* sth = (Tin*)(bt + C);  // staged theta, k, v of the next chunk: [16][D] each
+  float* scr = M + SM16_F;
+  float* U = scr + 5 * SM16_F;          // state group: U and the partial sums of Kt S
+  float* part = U + TILE_F;
+  Tin* sth = (Tin*)(part + 2 * TILE_F);  // prep group: staged theta, k, v of the next chunk
   Tin* sk = sth + C * D;
   Tin* sv = sk + C * D;
   const int tid = threadIdx.x;
+  const bool state_group = tid < kGroup;
+  const int gt = state_group ? tid : tid - kGroup;
   const int64_t b = chain / a.H;
   const int h = (int)(chain - b * a.H);
-  float* Sw = a.ws_S + (size_t)chain * a.nch * kStateF;
-  auto stage = [&](int n) -> float {  // issue chunk n's copies; returns its beta for this thread
-    const int nv = min(C, a.T - n * C);
-    const int64_t r0 = b * a.T + (int64_t)n * C;
-    stage_rows((const Tin*)a.theta, sth, a, r0, h, nv);
-    stage_rows((const Tin*)a.k, sk, a, r0, h, nv);
-    stage_rows((const Tin*)a.v, sv, a, r0, h, nv);
-    cp_async_commit();
-    return load_beta<Tin>(a, r0, h, nv);
-  };
+  auto Ktb = [&](int s_) { return buf + s_ * BUF_F; };
+  auto KhCb = [&](int s_) { return buf + s_ * BUF_F + TILE_F; };
+  auto Vb = [&](int s_) { return buf + s_ * BUF_F + 2 * TILE_F; };
+  auto Tbb = [&](int s_) { return buf + s_ * BUF_F + 3 * TILE_F; };
+  auto ecb = [&](int s_) { return buf + s_ * BUF_F + 3 * TILE_F + SM16_F; };
+  auto btb = [&](int s_) { return buf + s_ * BUF_F + 3 * TILE_F + SM16_F + D; };
 
-  float* RUw = a.ws_RU + (size_t)chain * a.nch * 2 * C * D;
-  float st[8][8];
-  state_load(st, a.init_state ? a.init_state + chain * kStateF : nullptr);
-  float bnext = stage(0);
-  for (int n = 0; n < a.nch; ++n) {
-    state_store(st, Sw + (size_t)n * kStateF, D);
-    state_store(st, S, LD);
-    const int t0 = n * C, nvalid = min(C, a.T - t0);
-    cp_async_wait_all();
-    __syncthreads();  // the staged chunk is complete, and the previous chunk's reads are done
-    load_chunk<Tin>(sth, sk, nullptr, sv, D, bnext, a.g_min, a.log_decay, nvalid, nullptr, Kt,
-                    1.0f, Kh, KhC, nullptr, nullptr, ec, bt, V);
-    __syncthreads();
-    if (n + 1 < a.nch) bnext = stage(n + 1);  // overlaps this chunk's products
-    {
-      const int m = tid >> 4, nn = tid & 15;
-      Ab[m * LS + nn] = nn < m ? dot128(Kt, m, Kh, nn) : 0.0f;
+  if (!state_group) {
+    // ---------------- prep group: chunk n's operands, Ab and the inverse
+    auto stage = [&](int n) -> float {  // issue chunk n's copies; returns its beta for this thread
+      const int nv = min(C, a.T - n * C);
+      const int64_t r0 = b * a.T + (int64_t)n * C;
+      stage_rows_group((const Tin*)a.theta, sth, a, r0, h, nv, gt);
+      stage_rows_group((const Tin*)a.k, sk, a, r0, h, nv, gt);
+      stage_rows_group((const Tin*)a.v, sv, a, r0, h, nv, gt);
+      cp_async_commit();
+      return load_beta<Tin>(a, r0, h, nv);  // thread kGroup + t holds beta_t
+    };
+    float bnext = stage(0);
+    for (int n = 0; n < a.nch; ++n) {
+      const int bs = n & 1;
+      const int nvalid = min(C, a.T - n * C);
+      if (n >= 2) bar_sync_all(BAR_FREE + bs);  // the state group is done with chunk n - 2
+      cp_async_wait_all();
+      bar_group(BAR_PG);  // the staged chunk is complete
+      prep_chunk<Tin>(sth, sk, sv, bnext, a.g_min, a.log_decay, nvalid, Ktb(bs), Kh, KhCb(bs),
+                      ecb(bs), btb(bs), Vb(bs), gt);
+      bar_group(BAR_PG);  // the staging reads are done and the tiles complete
+      if (n + 1 < a.nch) bnext = stage(n + 1);
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int e = gt + kGroup * e2, m = e >> 4, nn = e & 15;
+        Ab[m * LS + nn] = nn < m ? dot128(Ktb(bs), m, Kh, nn) : 0.0f;
+      }
+      bar_group(BAR_PG);
+      wy_inverse_group(Ab, btb(bs), M, Tbb(bs), scr, gt, BAR_PG);
+      bar_arrive_all(BAR_READY + bs);  // buffer bs holds chunk n
     }
-    __syncthreads();
-    wy_inverse(Ab, bt, M, Tb, nullptr, part);  // (the partial sums' tiles are free here)
-    __syncthreads();
-    part16<true>(Kt, S, part);  // Kt S
-    __syncthreads();
-    reduce_parts<C, 4>(part, V, V, -1.0f);  // R = V - Kt S
-    __syncthreads();
-    small16<false>(Tb, V, U, 1.0f);  // U = Tb R
-    __syncthreads();
+    return;
+  }
+
+  // ---------------- state group: S in registers (an 8 x 16 tile per thread)
+  float* Sw = a.ws_S + (size_t)chain * a.nch * kStateF;
+  float* RUw = a.ws_RU + (size_t)chain * a.nch * 2 * C * D;
+  float st[8][16];
+  group_state_load(st, a.init_state ? a.init_state + chain * kStateF : nullptr, gt);
+  for (int n = 0; n < a.nch; ++n) {
+    const int bs = n & 1;
+    float* Kt = Ktb(bs);
+    float* V = Vb(bs);
+    group_state_store(st, Sw + (size_t)n * kStateF, D, gt);
+    group_state_store(st, S, LD, gt);
+    bar_sync_all(BAR_READY + bs);  // chunk n's operands are ready; S is visible to the group
+    {
+      // Kt S as two partial sums over 64 key channels each
+      const int ng = gt & 31, mg = (gt >> 5) & 1, ks = gt >> 6;
+      float acc[8][4];
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[m][t] = 0.0f;
+      gemm_acc<8, 4, true, true>(acc, Kt, LD, 8 * mg, S, LD, 4 * ng, 0, 64 * ks, 64 * ks + 64);
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+        *(float4*)(part + (ks * C + 8 * mg + m) * LD + 4 * ng) =
+            make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+    }
+    bar_group(BAR_SG);
+    for (int e = gt; e < C * D / 4; e += kGroup) {  // R = V - Kt S, in place of V
+      const int m = e >> 5, nn = (e & 31) * 4;
+      const float4 p0 = *(const float4*)(part + m * LD + nn);
+      const float4 p1 = *(const float4*)(part + (C + m) * LD + nn);
+      float4 r = *(const float4*)(V + m * LD + nn);
+      r.x = fmaf(-1.0f, p0.x + p1.x, r.x);
+      r.y = fmaf(-1.0f, p0.y + p1.y, r.y);
+      r.z = fmaf(-1.0f, p0.z + p1.z, r.z);
+      r.w = fmaf(-1.0f, p0.w + p1.w, r.w);
+      *(float4*)(V + m * LD + nn) = r;
+    }
+    bar_group(BAR_SG);
+    {
+      // U = Tb R: rows 4 mg .. 4 mg + 3, columns 4 ng .. 4 ng + 3
+      const int ng = gt & 31, mg = gt >> 5;
+      float acc[4][4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[m][t] = 0.0f;
+      gemm_acc<4, 4, true, true>(acc, Tbb(bs), LS, 4 * mg, V, LD, 4 * ng, 0, 0, C);
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        *(float4*)(U + (4 * mg + m) * LD + 4 * ng) = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+    }
+    bar_group(BAR_SG);
     // R and U of the chunk for the gradient kernel
-    for (int e = tid; e < 2 * C * D / 4; e += kThreads) {
+    for (int e = gt; e < 2 * C * D / 4; e += kGroup) {
       const int t = (e >> 5) & (C - 1), c = (e & 31) * 4;
       const float* src = (e < C * D / 4 ? V : U) + t * LD + c;
       *(float4*)(RUw + (size_t)n * 2 * C * D + (e >> 5) * D + c) = *(const float4*)src;
     }
-    // the last chunk's end state is not needed
-    if (n + 1 < a.nch) state_update<C>(st, ec, KhC, U);  // S' = Diag(ec) S + KhC^T U
+    if (n + 1 < a.nch) {
+      // S' = Diag(ec) S + KhC^T U (the last chunk's end state is not needed)
+      const int ig = gt >> 3, jg = gt & 7;
+      const float* ec = ecb(bs);
+      const float* KhC = KhCb(bs);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float e = ec[8 * ig + i];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) st[i][j] *= e;
+      }
+#pragma unroll 4
+      for (int k = 0; k < C; ++k) {
+        const float4 a0 = *(const float4*)(KhC + k * LD + 8 * ig);
+        const float4 a1 = *(const float4*)(KhC + k * LD + 8 * ig + 4);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float4 bv = *(const float4*)(U + k * LD + 32 * g + 4 * jg);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            ffma2(st[i][4 * g], st[i][4 * g + 1], av[i], bv.x, bv.y);
+            ffma2(st[i][4 * g + 2], st[i][4 * g + 3], av[i], bv.z, bv.w);
+          }
+        }
+      }
+    }
+    // buffer bs may take chunk n + 2 (the prep group waits for this only then)
+    if (n + 2 < a.nch) bar_arrive_all(BAR_FREE + bs);
   }
 }
 
@@ -948,7 +1208,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
 
 template <typename Tin>
 constexpr size_t smem_states() {
-  return (size_t)(STATE_F + 9 * TILE_F + 3 * SM16_F + D + C) * 4 + 3 * C * D * sizeof(Tin);
+  return (size_t)(STATE_F + 2 * BUF_F + TILE_F + 7 * SM16_F + TILE_F + 2 * TILE_F) * 4 +
+         3 * C * D * sizeof(Tin);
 }
 template <typename Tin>
 constexpr size_t smem_reverse() {
