@@ -396,21 +396,6 @@ __device__ __forceinline__ void cp_async_wait_one_pending() {
   asm volatile("cp.async.wait_group 1;" ::: "memory");
 }
 
-// Rows row0 .. row0 + 15 of head h of a [tokens, H, D] tensor into a dense
-// [16][D] shared tile with cp.async (rows past nvalid zero-filled).
-template <typename T>
-__device__ __forceinline__ void stage_rows(const T* g, T* s, const BwdDev& a, int64_t row0, int h,
-                                           int nvalid) {
-  constexpr int kUnits = (int)(D * sizeof(T) / 16);  // 16-byte pieces per row
-  constexpr int kElems = (int)(16 / sizeof(T));
-  const T* g0 = g + (row0 * a.H + h) * D;
-  for (int u = threadIdx.x; u < C * kUnits; u += kThreads) {
-    const int t = u / kUnits, o = (u % kUnits) * kElems;
-    const bool ok = t < nvalid;
-    cp_async16(s + t * D + o, (ok ? g0 + (int64_t)t * a.H * D : g0) + o, ok);
-  }
-}
-
 // M = (I + N)^{-1} with N = Diag(b) Ab strictly lower, Tb = M Diag(b), and the
 // transpose of Tb when asked.  N is nilpotent (N^16 = 0), so
 //   (I + N)^{-1} = (I - N)(I + N^2)(I + N^4)(I + N^8),
@@ -503,20 +488,6 @@ __device__ __forceinline__ void state_load(float (&st)[8][8], const float* src) 
     }
 }
 
-// st <- Diag(ec) st + A^T B over K token rows (A, B row-major token tiles).
-template <int K>
-__device__ __forceinline__ void state_update(float (&st)[8][8], const float* ec, const float* A,
-                                             const float* B) {
-  const int ig = threadIdx.x >> 4, jg = threadIdx.x & 15;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float e = ec[8 * ig + i];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) st[i][j] *= e;
-  }
-  gemm_acc<8, 8, false, true>(st, A, LD, 8 * ig, B, LD, 4 * jg, 64, 0, K);
-}
-
 // ------------------------------------------------------- forward recurrence
 // Warp-specialised: warps 0..3 (the state group) carry S and run the products
 // that need it; warps 4..7 (the prep group) form the next chunk's operands --
@@ -590,7 +561,8 @@ __device__ __forceinline__ void prep_chunk(const Tin* th0, const Tin* k0, const 
 // barrier between the rounds.  M and Tb are complete after the group's next
 // barrier.
 __device__ __forceinline__ void wy_inverse_group(const float* Ab, const float* bt, float* M,
-                                                 float* Tb, float* scratch, int gt, int bar) {
+                                                 float* Tb, float* TbT, float* scratch, int gt,
+                                                 int bar) {
   const int i0 = gt >> 4, j = gt & 15;
   float* B0 = scratch;
   float* B1 = B0 + SM16_F;
@@ -649,6 +621,7 @@ __device__ __forceinline__ void wy_inverse_group(const float* Ab, const float* b
     for (int l = 0; l < C; ++l) q = fmaf(B1[i * LS + l], B0[l * LS + j], q);
     M[ij] = q;
     Tb[ij] = q * bj;
+    if (TbT) TbT[j * LS + i] = q * bj;
   }
 }
 
@@ -750,7 +723,7 @@ __device__ __forceinline__ void states_chain(const BwdDev& a, int64_t chain) {
         Ab[m * LS + nn] = nn < m ? dot128(Ktb(bs), m, Kh, nn) : 0.0f;
       }
       bar_group(BAR_PG);
-      wy_inverse_group(Ab, btb(bs), M, Tbb(bs), scr, gt, BAR_PG);
+      wy_inverse_group(Ab, btb(bs), M, Tbb(bs), nullptr, scr, gt, BAR_PG);
       bar_arrive_all(BAR_READY + bs);  // buffer bs holds chunk n
     }
     return;
@@ -848,86 +821,236 @@ __device__ __forceinline__ void states_chain(const BwdDev& a, int64_t chain) {
 }
 
 // ------------------------------------------------------- reverse recurrence
+// Warp-specialised like the forward recurrence: the prep group forms chunk n's
+// operands -- Qt, -Kt, Kh, KhC, dO, Ab, Pi^T, the inverse and Pi^T dO, none of
+// which needs dS -- while the state group runs chunk n + 1's products with dS.
+
+// The reverse recurrence's per-channel operands (prep group, one channel per
+// thread): Qt = Q e^{G}, -Kt, Kh, KhC and e^{G_C} by the products of
+// prep_chunk, and the chunk's d_out rows from the staged copy.
+template <typename Tin>
+__device__ __forceinline__ void prep_chunk_rev(const Tin* th0, const Tin* k0, const Tin* q0,
+                                               const float* sdo, float bval, float g_min,
+                                               int log_decay, int nvalid, float* Qt, float* mKt,
+                                               float* Kh, float* KhC, float* dO, float* ec,
+                                               float* bt, int gt) {
+  const int c = gt;
+  float xr[C], kr[C], qr[C], egr[C];
+#pragma unroll
+  for (int t = 0; t < C; ++t) {
+    const bool ok = t < nvalid;
+    xr[t] = ok ? to_f32(th0[t * D + c]) : 0.0f;
+    kr[t] = ok ? to_f32(k0[t * D + c]) : 0.0f;
+    qr[t] = ok ? to_f32(q0[t * D + c]) : 0.0f;
+  }
+  float E = 1.0f, Ei = 1.0f;
+#pragma unroll
+  for (int t = 0; t < C; ++t) {
+    float g = 0.0f;
+    if (t < nvalid) {
+      if (log_decay) {
+        g = xr[t];
+      } else {
+        const float x = xr[t];
+        const float e = expf(-fabsf(x));
+        const float big = 1.0f / (1.0f + e), small = e * big;
+        g = g_min * (x >= 0.0f ? big : small);
+      }
+    }
+    const float eg = expf(g);
+    E *= eg;
+    Ei *= 1.0f / eg;
+    egr[t] = eg;
+    Qt[t * LD + c] = qr[t] * E;
+    mKt[t * LD + c] = -(kr[t] * E);
+    Kh[t * LD + c] = kr[t] * Ei;
+    dO[t * LD + c] = sdo[t * D + c];
+  }
+  ec[c] = E;
+  float P = 1.0f;
+#pragma unroll
+  for (int t = C - 1; t >= 0; --t) {
+    KhC[t * LD + c] = kr[t] * P;
+    P *= egr[t];
+  }
+  if (gt < C) bt[gt] = bval;
+}
+
+// one prep buffer of the reverse recurrence: [Qt; -Kt], [dO; dR], KhC, dU,
+// Tb^T, e^{G_C}, beta
+constexpr int BUF_R = 6 * TILE_F + SM16_F + D + C;
+static_assert(BUF_R % 4 == 0, "prep buffers on 16-byte boundaries");
+
 template <typename Tin>
 __device__ __forceinline__ void reverse_chain(const BwdDev& a, int64_t chain) {
   extern __shared__ __align__(16) float smf[];
-  float* dS = smf;
-  float* Qt = dS + STATE_F;  // [Qt; -Kt]: 32 rows
-  float* mKt = Qt + TILE_F;
-  float* Kh = mKt + TILE_F;
-  float* KhC = Kh + TILE_F;
-  float* dO = KhC + TILE_F;  // [dO; dR]: 32 rows
-  float* dR = dO + TILE_F;
-  float* dU = dR + TILE_F;
-  float* part = dU + TILE_F;  // 4 tiles
-  float* Ab = part + 4 * TILE_F;
+  float* dS = smf;                       // the state group's copy of dS' for KhC dS'
+  float* buf = dS + STATE_F;             // two prep buffers
+  float* Kh = buf + 2 * BUF_R;           // prep group: Kh, Ab, Pi^T, M, Tb, inverse scratch
+  float* Ab = Kh + TILE_F;
   float* PiT = Ab + SM16_F;
   float* M = PiT + SM16_F;
   float* Tb = M + SM16_F;
-  float* TbT = Tb + SM16_F;
-  float* ec = TbT + SM16_F;
-  float* bt = ec + D;
-  float* sdo = bt + C;  // staged d_out, theta, k, q of the next chunk: [16][D] each
+  float* scr = Tb + SM16_F;
+  float* sdo = scr + 5 * SM16_F;         // prep group: staged d_out, theta, k, q of the next chunk
   Tin* sth = (Tin*)(sdo + C * D);
   Tin* sk = sth + C * D;
   Tin* sq = sk + C * D;
   const int tid = threadIdx.x;
+  const bool state_group = tid < kGroup;
+  const int gt = state_group ? tid : tid - kGroup;
   const int64_t b = chain / a.H;
   const int h = (int)(chain - b * a.H);
+  auto Qtb = [&](int s_) { return buf + s_ * BUF_R; };                 // then -Kt
+  auto dOb = [&](int s_) { return buf + s_ * BUF_R + 2 * TILE_F; };    // then dR
+  auto KhCb = [&](int s_) { return buf + s_ * BUF_R + 4 * TILE_F; };
+  auto dUb = [&](int s_) { return buf + s_ * BUF_R + 5 * TILE_F; };
+  auto TbTb = [&](int s_) { return buf + s_ * BUF_R + 6 * TILE_F; };
+  auto ecb = [&](int s_) { return buf + s_ * BUF_R + 6 * TILE_F + SM16_F; };
+  auto btb = [&](int s_) { return buf + s_ * BUF_R + 6 * TILE_F + SM16_F + D; };
+
+  if (!state_group) {
+    // ---------------- prep group, chunks from the last to the first
+    auto stage = [&](int n) -> float {  // issue chunk n's copies; returns its beta for this thread
+      const int nv = min(C, a.T - n * C);
+      const int64_t r0 = b * a.T + (int64_t)n * C;
+      stage_rows_group(a.d_out, sdo, a, r0, h, nv, gt);
+      stage_rows_group((const Tin*)a.theta, sth, a, r0, h, nv, gt);
+      stage_rows_group((const Tin*)a.k, sk, a, r0, h, nv, gt);
+      stage_rows_group((const Tin*)a.q, sq, a, r0, h, nv, gt);
+      cp_async_commit();
+      return load_beta<Tin>(a, r0, h, nv);  // thread kGroup + t holds beta_t
+    };
+    float bnext = stage(a.nch - 1);
+    for (int i = 0; i < a.nch; ++i) {
+      const int n = a.nch - 1 - i, bs = i & 1;
+      const int nvalid = min(C, a.T - n * C);
+      float* Qt = Qtb(bs);
+      float* dO = dOb(bs);
+      if (i >= 2) bar_sync_all(BAR_FREE + bs);  // the state group is done with chunk n + 2
+      cp_async_wait_all();
+      bar_group(BAR_PG);  // the staged chunk is complete
+      prep_chunk_rev<Tin>(sth, sk, sq, sdo, bnext, a.g_min, a.log_decay, nvalid, Qt, Qt + TILE_F, Kh,
+                          KhCb(bs), dO, ecb(bs), btb(bs), gt);
+      bar_group(BAR_PG);  // the staging reads are done and the tiles complete
+      if (n > 0) bnext = stage(n - 1);
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int e = gt + kGroup * e2, m = e >> 4, nn = e & 15;
+        Ab[m * LS + nn] = nn < m ? -dot128(Qt + TILE_F, m, Kh, nn) : 0.0f;
+        PiT[nn * LS + m] = nn <= m ? dot128(Qt, m, Kh, nn) : 0.0f;
+      }
+      bar_group(BAR_PG);
+      {
+        // Pi^T dO, the part of dU that does not involve dS'
+        const int ng = gt & 31, mg = gt >> 5;
+        float acc[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+          for (int t = 0; t < 4; ++t) acc[m][t] = 0.0f;
+        gemm_acc<4, 4, true, true>(acc, PiT, LS, 4 * mg, dO, LD, 4 * ng, 0, 0, C);
+        float* dU = dUb(bs);
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          *(float4*)(dU + (4 * mg + m) * LD + 4 * ng) =
+              make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+      }
+      wy_inverse_group(Ab, btb(bs), M, Tb, TbTb(bs), scr, gt, BAR_PG);
+      bar_arrive_all(BAR_READY + bs);  // buffer bs holds chunk n
+    }
+    return;
+  }
+
+  // ---------------- state group: dS in registers (an 8 x 16 tile per thread)
   float* dSw = a.ws_dS + (size_t)chain * a.nch * kStateF;
   float* dUw = a.ws_dU + (size_t)chain * a.nch * C * D;
-  auto stage = [&](int n) -> float {  // issue chunk n's copies; returns its beta for this thread
-    const int nv = min(C, a.T - n * C);
-    const int64_t r0 = b * a.T + (int64_t)n * C;
-    stage_rows(a.d_out, sdo, a, r0, h, nv);
-    stage_rows((const Tin*)a.theta, sth, a, r0, h, nv);
-    stage_rows((const Tin*)a.k, sk, a, r0, h, nv);
-    stage_rows((const Tin*)a.q, sq, a, r0, h, nv);
-    cp_async_commit();
-    return load_beta<Tin>(a, r0, h, nv);
-  };
-
-  float st[8][8];
-  state_load(st, a.d_final ? a.d_final + chain * kStateF : nullptr);
-  float bnext = stage(a.nch - 1);
-  for (int n = a.nch - 1; n >= 0; --n) {
-    state_store(st, dSw + (size_t)n * kStateF, D);
-    state_store(st, dS, LD);
+  float st[8][16];
+  group_state_load(st, a.d_final ? a.d_final + chain * kStateF : nullptr, gt);
+  for (int i = 0; i < a.nch; ++i) {
+    const int n = a.nch - 1 - i, bs = i & 1;
     const int t0 = n * C, nvalid = min(C, a.T - t0);
     const int64_t row0 = b * a.T + t0;
-    cp_async_wait_all();
-    __syncthreads();  // the staged chunk is complete, and the previous chunk's reads are done
-    load_chunk<Tin>(sth, sk, sq, nullptr, D, bnext, a.g_min, a.log_decay, nvalid, Qt, mKt, -1.0f,
-                    Kh, KhC, nullptr, nullptr, ec, bt, nullptr);
-    for (int e = tid; e < C * D; e += kThreads) dO[(e >> 7) * LD + (e & (D - 1))] = sdo[e];
-    __syncthreads();
-    if (n > 0) bnext = stage(n - 1);  // overlaps this chunk's products
+    float* dU = dUb(bs);
+    float* dR = dOb(bs) + TILE_F;
+    group_state_store(st, dSw + (size_t)n * kStateF, D, gt);
+    group_state_store(st, dS, LD, gt);
+    bar_sync_all(BAR_READY + bs);  // chunk n's operands are ready; dS' is visible to the group
+    const int ng = gt & 31, mg = gt >> 5;
     {
-      const int m = tid >> 4, nn = tid & 15;
-      Ab[m * LS + nn] = nn < m ? -dot128(mKt, m, Kh, nn) : 0.0f;
-      PiT[nn * LS + m] = nn <= m ? dot128(Qt, m, Kh, nn) : 0.0f;
+      // dU = Pi^T dO + KhC dS'
+      float acc[4][4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[m][t] = 0.0f;
+      gemm_acc<4, 4, true, true>(acc, KhCb(bs), LD, 4 * mg, dS, LD, 4 * ng, 0, 0, D);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        float4* o = (float4*)(dU + (4 * mg + m) * LD + 4 * ng);
+        float4 r = *o;
+        r.x = fmaf(1.0f, acc[m][0], r.x);
+        r.y = fmaf(1.0f, acc[m][1], r.y);
+        r.z = fmaf(1.0f, acc[m][2], r.z);
+        r.w = fmaf(1.0f, acc[m][3], r.w);
+        *o = r;
+      }
     }
-    __syncthreads();
-    wy_inverse(Ab, bt, M, Tb, TbT, part);  // (the partial sums' tiles are free here)
-    __syncthreads();
-    part16<true>(KhC, dS, part);  // KhC dS'
-    small16<false>(PiT, dO, dU, 1.0f);  // Pi^T dO
-    __syncthreads();
-    reduce_parts<C, 4>(part, dU, dU, 1.0f);  // dU = Pi^T dO + KhC dS'
-    __syncthreads();
-    for (int e = tid; e < C * D / 4; e += kThreads) {
+    bar_group(BAR_SG);
+    for (int e = gt; e < C * D / 4; e += kGroup) {
       const int t = e >> 5, c = (e & 31) * 4;
       *(float4*)(dUw + (size_t)n * C * D + t * D + c) = *(const float4*)(dU + t * LD + c);
     }
-    small16<false>(TbT, dU, dR, 1.0f);  // dR = Tb^T dU
-    __syncthreads();
-    for (int e = tid; e < C * D; e += kThreads) {
+    {
+      // dR = Tb^T dU
+      float acc[4][4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc[m][t] = 0.0f;
+      gemm_acc<4, 4, true, true>(acc, TbTb(bs), LS, 4 * mg, dU, LD, 4 * ng, 0, 0, C);
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        *(float4*)(dR + (4 * mg + m) * LD + 4 * ng) =
+            make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+    }
+    bar_group(BAR_SG);
+    for (int e = gt; e < C * D; e += kGroup) {
       const int t = e >> 7, c = e & (D - 1);
       if (t < nvalid) a.dv[((row0 + t) * a.H + h) * D + c] = dR[t * LD + c];
     }
-    state_update<2 * C>(st, ec, Qt, dO);  // dS = Diag(ec) dS' + [Qt; -Kt]^T [dO; dR]
+    {
+      // dS = Diag(ec) dS' + [Qt; -Kt]^T [dO; dR]
+      const int ig = gt >> 3, jg = gt & 7;
+      const float* ec = ecb(bs);
+      const float* A = Qtb(bs);
+      const float* B = dOb(bs);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float e = ec[8 * ig + r];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) st[r][j] *= e;
+      }
+#pragma unroll 4
+      for (int k = 0; k < 2 * C; ++k) {
+        const float4 a0 = *(const float4*)(A + k * LD + 8 * ig);
+        const float4 a1 = *(const float4*)(A + k * LD + 8 * ig + 4);
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float4 bv = *(const float4*)(B + k * LD + 32 * g + 4 * jg);
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            ffma2(st[r][4 * g], st[r][4 * g + 1], av[r], bv.x, bv.y);
+            ffma2(st[r][4 * g + 2], st[r][4 * g + 3], av[r], bv.z, bv.w);
+          }
+        }
+      }
+    }
+    // buffer bs may take chunk n - 2 (the prep group waits for this only then)
+    if (i + 2 < a.nch) bar_arrive_all(BAR_FREE + bs);
   }
-  if (a.d_init) state_store(st, a.d_init + chain * kStateF, D);
+  if (a.d_init) group_state_store(st, a.d_init + chain * kStateF, D, gt);
 }
 
 // The two recurrences are independent of each other and run as one grid: CTAs
@@ -1213,7 +1336,7 @@ constexpr size_t smem_states() {
 }
 template <typename Tin>
 constexpr size_t smem_reverse() {
-  return (size_t)(STATE_F + 11 * TILE_F + 5 * SM16_F + D + C + C * D) * 4 + 3 * C * D * sizeof(Tin);
+  return (size_t)(STATE_F + 2 * BUF_R + TILE_F + 9 * SM16_F + C * D) * 4 + 3 * C * D * sizeof(Tin);
 }
 constexpr size_t kSmemGrads = (size_t)(STATE_F + 16 * TILE_F + 11 * SM16_F + 2 * D + 3 * C) * 4;
 static_assert(kSmemGrads <= 232448 && smem_reverse<float>() <= 232448 &&
