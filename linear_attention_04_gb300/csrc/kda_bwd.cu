@@ -34,8 +34,8 @@
 // The recurrences carry their 128 x 128 state in registers with a copy in
 // shared memory for the products that contract over it, and stage the next
 // chunk's inputs in shared memory with cp.async while the current chunk
-// computes.  The forward recurrence is warp-specialised: four warps form the
-// next chunk's operands while the other four run the current chunk's state
+// computes.  Both recurrences are warp-specialised: four warps form the next
+// chunk's operands while the other four run the current chunk's state
 // products.  Every product is an fp32 FMA over shared-memory operands.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
