@@ -610,10 +610,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) KTRACE(n, 7);
       auto refill = [&]() {
         if (n + kIntraWarps < nchunks) {
-          if (lane == 0) {
-            fence_proxy_async_smem();
-            load(n + kIntraWarps);
-          }
+          // the stage was only read (every value loaded from it has been used
+          // by now, and __syncwarp orders the lanes' reads before this point),
+          // so the copy that overwrites it needs no proxy fence
+          if (lane == 0) load(n + kIntraWarps);
           ++issued;
         }
       };
