@@ -950,6 +950,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nvalid = (*sflags & kJobNoOut) ? 0 : min(C, L - n * C);
         const int64_t row0 = ch.t0 + (int64_t)n * C;
         {
+        // the four token rows this lane writes (j, c & 1), as element offsets of
+        // its first channel; the channels then differ by constants
+        int64_t rowoff[2][2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            rowoff[j][e] = ((row0 + 8 * j + 2 * q + e) * H + h) * D + kDvPerWarp * sw + g;
 #pragma unroll
         for (int m = 0; m < kMT; ++m)
 #pragma unroll
@@ -957,11 +965,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const int r = 8 * j + 2 * q + (c & 1);
-              const int dv = kDvPerWarp * sw + 16 * m + g + 8 * (c >> 1);
               const float dcr = j ? ((c & 1) ? dc1.y : dc1.x) : ((c & 1) ? dc0.y : dc0.x);
               const float o = accO[m][j][c] + dcr * accU[m][j][c];
               if (r < nvalid) {
-                const int64_t idx = ((row0 + r) * H + h) * D + dv;
+                const int64_t idx = rowoff[j][c & 1] + 16 * m + 8 * (c >> 1);
                 if constexpr (kOutBf16)
                   ((__nv_bfloat16*)args.out)[idx] = __float2bfloat16_rn(o);
                 else
