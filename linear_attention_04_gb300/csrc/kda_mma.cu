@@ -58,6 +58,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kda_device.cuh"
@@ -126,14 +127,18 @@ struct Lay {
   static constexpr int B_FREE = B_READY + kSlots;            // [kSlots] state warps (4 arrivals)
   static constexpr int B_GRAM = B_FREE + kSlots;             // [kIntraWarps] Gram product done
   static constexpr int NBARS = B_GRAM + (kTc ? kIntraWarps : 0);
-  static constexpr uint32_t MISC = BARS + NBARS * 8;         // abort, job flags, tensor memory address
-  static constexpr uint32_t RANK = kTc ? GA : MISC + 16;     // chain-order scratch
-  static constexpr uint32_t TOTAL = kTc ? MISC + 16 : RANK + (kMaxRankedSeqsDev + 1) * 4;
+  // abort, job flags, tensor memory address (16 bytes), then the CTA's chunk
+  // schedule (64 bytes)
+  static constexpr uint32_t MISC = BARS + NBARS * 8;
+  static constexpr uint32_t SCHED = MISC + 16;
+  static constexpr uint32_t RANK = kTc ? GA : MISC + 80;     // chain-order scratch
+  static constexpr uint32_t TOTAL = kTc ? MISC + 80 : RANK + (kMaxRankedSeqsDev + 1) * 4;
   static constexpr uint32_t BYTES = TOTAL + (kTc ? 1024 : 128);  // + alignment slack
   static_assert(BYTES <= 232448, "shared memory budget");
   static_assert(SLOT_BYTES % 128 == 0 && SLOTS % 128 == 0, "slot alignment");
   static_assert(KH % 1024 == 0 && GA % 1024 == 0, "swizzled operand tiles on 1024-byte boundaries");
   static_assert(!kTc || (kMaxRankedSeqsDev + 1) * 4 <= GA_BYTES, "chain-order scratch fits the tile");
+  static_assert(MISC % 8 == 0, "schedule alignment");
 };
 
 // Byte offset of (row, col) in a tile of 256-byte rows (128 bf16 channels)
@@ -317,6 +322,14 @@ __device__ __forceinline__ void position_wise_tiles(const unsigned char* st, uns
 struct MmaArgs {
   const SegJob* jobs;  // per-CTA work units (segmented launches), or null
   uint64_t wait_ns;    // limit of every bounded wait
+  // Wrapped schedule (kWrap launches: fixed-length batches with more chains
+  // than resident CTAs): CTA b runs chunk steps [b wrap_cap, (b + 1) wrap_cap)
+  // of the chains laid end to end; a chain cut by a window boundary hands its
+  // state over through its final_state slot, announced by a per-warp flag set
+  // to `epoch`.
+  int wrap_cap;
+  uint32_t epoch;
+  uint32_t* hflags;  // [grid + 1][kStateWarps] handoff flags of this launch
   const __nv_bfloat16* beta;
   float g_min;
   int gate;
@@ -328,6 +341,158 @@ struct MmaArgs {
   int N, H, T;
   int* status;
 };
+
+// The chunk steps 0 .. nsteps-1 of one CTA.
+// Unwrapped: chunks 0 .. nsteps-1 of one chain (first token row `row`, head
+// `head`, `len` tokens).
+// Wrapped: positions [w0, w0 + nsteps) of the N H chains of p chunks each laid
+// end to end (chain c = sequence c / H, head c mod H, T tokens from row
+// (c / H) T).  A chain cut by the window's start runs its first `a` chunks
+// here, at the start, and the rest at the end of the previous CTA's window; a
+// chain cut by the window's end runs its last `y` chunks here, at the end,
+// from the state that the next CTA hands over after running its first
+// chunks.  With every window at least p long, the first part of a cut chain
+// ends (a chunk-steps into the later window) well before its second part
+// starts (p - a chunk-steps before the earlier window's end), so the hand-over
+// costs no waiting (McNaughton's wrap-around rule, with each cut chain's two
+// parts in the order the recurrence needs).
+struct Sched {
+  int wrap, nsteps;
+  int64_t row;   // unwrapped
+  int64_t soff;  // unwrapped: element offset of the chain's states in init/final
+  int head, len;
+  int w0, a, y, p, H, T;  // wrapped
+};
+
+static_assert(sizeof(Sched) <= 64, "the schedule's shared-memory slot");
+
+// One chain's run of consecutive steps starting at step n.
+struct Piece {
+  int64_t chain;     // chain index (wrapped); its states sit at chain * D * D
+  int64_t row;       // token row of the chain's first token
+  int head, len;     // head; tokens of the chain
+  int nc0, steps;    // chunk of the chain at the piece's first step; steps
+  bool from_handoff;  // start state handed over by the next CTA
+  bool to_handoff;    // end state handed over to the previous CTA
+};
+
+__device__ __forceinline__ int sched_chain(const volatile Sched& s, int n, int& nc) {
+  int c;
+  if (n < s.a) {
+    c = s.w0 / s.p;
+    nc = n;
+  } else if (n < s.nsteps - s.y) {
+    const int v = s.w0 + n;
+    c = v / s.p;
+    nc = v - c * s.p;
+  } else {
+    c = (s.w0 + s.nsteps) / s.p;
+    nc = n - s.nsteps + s.p;
+  }
+  return c;
+}
+
+// The chunk at one step, as an intra warp walks the schedule.
+struct Cursor {
+  int64_t row;  // token row of the chunk's first token
+  int head;
+  int rem;      // tokens of the chain from this chunk on (valid rows: min(C, rem))
+  int pend;     // first step after the piece that holds this step
+};
+
+__device__ __forceinline__ Cursor cursor_at(const volatile Sched& s, int n) {
+  Cursor k;
+  if (!s.wrap) {
+    k.row = s.row + (int64_t)n * C;
+    k.head = s.head;
+    k.rem = s.len - n * C;
+    k.pend = s.nsteps;
+    return k;
+  }
+  int nc;
+  const int c = sched_chain(s, n, nc);
+  const int seq = c / s.H;
+  k.head = c - seq * s.H;
+  k.row = (int64_t)seq * s.T + (int64_t)nc * C;
+  k.rem = s.T - nc * C;
+  if (n < s.a)
+    k.pend = s.a;
+  else if (n < s.nsteps - s.y)
+    k.pend = n - nc + s.p;
+  else
+    k.pend = s.nsteps;
+  return k;
+}
+
+// The cursor `step` steps after the cursor k of step n: the same chain while
+// the piece lasts (no division), else looked up afresh.
+__device__ __forceinline__ Cursor cursor_next(const volatile Sched& s, const Cursor& k, int n,
+                                              int step) {
+  if (n + step < k.pend) {
+    Cursor r = k;
+    r.row += (int64_t)step * C;
+    r.rem -= step * C;
+    return r;
+  }
+  return cursor_at(s, n + step);
+}
+
+template <bool kMayWrap>
+__device__ __forceinline__ Piece sched_piece(const volatile Sched& s, int n) {
+  Piece pc;
+  pc.from_handoff = pc.to_handoff = false;
+  if (!kMayWrap || !s.wrap) {
+    pc.chain = 0;
+    pc.row = s.row;
+    pc.head = s.head;
+    pc.len = s.len;
+    pc.nc0 = 0;
+    pc.steps = s.nsteps;
+    return pc;
+  }
+  int nc;
+  const int c = sched_chain(s, n, nc);
+  pc.nc0 = nc;
+  if (n < s.a) {
+    pc.steps = s.a;
+    pc.to_handoff = true;
+  } else if (n < s.nsteps - s.y) {
+    pc.steps = s.p;
+  } else {
+    pc.steps = s.y;
+    pc.from_handoff = true;
+  }
+  const int seq = c / s.H;
+  pc.chain = c;
+  pc.head = c - seq * s.H;
+  pc.row = (int64_t)seq * s.T;
+  pc.len = s.T;
+  return pc;
+}
+
+// Acquire / release accesses of the hand-over flags (gpu scope).
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Waits until *f == want; gives up after limit_ns or once *abort is set.
+__device__ __forceinline__ bool wait_flag(const uint32_t* f, uint32_t want, const volatile int* abort,
+                                          uint64_t limit_ns) {
+  if (ld_acquire_u32(f) == want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(256);
+    if (ld_acquire_u32(f) == want) return true;
+    if ((i & 15) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
 
 // Optional event trace of the first CTA (compile with -DKDA_TRACE): wall-clock
 // time of each pipeline event per chunk, read back with kda_debug_trace_read_mma.
@@ -359,7 +524,9 @@ __device__ __forceinline__ void fail(volatile int* abort, int* status) {
 // kFallback: compile the position-wise fallback for chunks whose decay is too
 // steep for the dense tile (only a given, unbounded log-decay can produce
 // them; the bounded gate's kernel carries no such code)
-template <bool kOutBf16, bool kFallback, bool kTc>
+// kWrap: the wrapped schedule (one window of chunk steps per CTA); otherwise
+// one chain (or one segment job) per CTA.
+template <bool kOutBf16, bool kFallback, bool kTc, bool kWrap>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_fwd_mma_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -379,7 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ldmatrix.x4 (mi: which 8x8 matrix this lane addresses, rr: its row)
   const int g = lane >> 2, q = lane & 3, mi = lane >> 3, rr = lane & 7;
 
-  // the work unit: a whole (sequence, head) chain, or one segment job
+  // the work unit: a whole (sequence, head) chain, one segment job, or one
+  // window of the wrapped schedule.  (The wrapped instantiation tests the
+  // schedule at run time, as one flag it cannot fold: its register allocation
+  // then measures faster than with the choice folded in.)
+  const bool wrap_rt = kWrap && args.wrap_cap > 0;
   Chain ch;
   int flags = 0;
   const float* init_state = args.init_state;
@@ -394,6 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     flags = jb.flags;
     init_state = jb.init;
     final_state = jb.final_state;
+  } else if (wrap_rt) {
+    ch.seq = ch.head = 0;
+    ch.t0 = ch.t1 = 0;
+    ch.valid = true;
   } else {
     ch = chain_for_block(blockIdx.x, args.H, args.N, args.T, args.cu_seqlens, (int*)(sm + Ly::RANK));
     if (!ch.valid) {
@@ -406,10 +581,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   // options read back from shared memory where they are used (keeps them out
   // of the register budget of the main loops)
   volatile int* sflags = (volatile int*)(sm + Ly::MISC + 4);
-  const int h = ch.head;
   const int H = args.H;
-  const int L = (int)(ch.t1 - ch.t0);
-  const int nchunks = (L + C - 1) / C;
+  // the CTA's chunk schedule, kept in shared memory and read where it is used
+  // (out of the register budget of the main loops)
+  volatile Sched& sc = *(volatile Sched*)(sm + Ly::SCHED);
+  int nsteps;
+  if (tid == 0) {
+    Sched s = {};
+    s.wrap = wrap_rt;
+    if (wrap_rt) {
+      s.p = (args.T + C - 1) / C;
+      s.H = args.H;
+      s.T = args.T;
+      const int total = args.N * args.H * s.p;  // below 2^31 (checked by the host)
+      s.w0 = (int)blockIdx.x * args.wrap_cap;
+      s.nsteps = min(args.wrap_cap, total - s.w0);
+      const int x = s.w0 % s.p;
+      s.a = x ? s.p - x : 0;
+      const int w1 = s.w0 + s.nsteps;
+      s.y = w1 < total ? w1 % s.p : 0;
+    } else {
+      s.row = ch.t0;
+      s.soff = soff;
+      s.head = ch.head;
+      s.len = (int)(ch.t1 - ch.t0);
+      s.nsteps = (s.len + C - 1) / C;
+    }
+    sc.wrap = s.wrap;
+    sc.nsteps = s.nsteps;
+    sc.row = s.row;
+    sc.soff = s.soff;
+    sc.head = s.head;
+    sc.len = s.len;
+    sc.w0 = s.w0;
+    sc.a = s.a;
+    sc.y = s.y;
+    sc.p = s.p;
+    sc.H = s.H;
+    sc.T = s.T;
+  }
 
   if constexpr (kTc) {
     // tensor memory for the intra products: 16 columns per intra warp
@@ -426,6 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if constexpr (kTc) tc_fence_after();
   const uint32_t sbase = smem_u32(sm);
+  nsteps = sc.nsteps;
 
   if (warp >= kStateWarps) {
     // ================================================================ intra warps
@@ -437,26 +648,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* ab = (float*)(sm + Ly::AB + iw * AB_BYTES);
     uint64_t* full = &bars[Ly::B_FULL + iw];
     const bool zero_v = *sflags & kJobZeroV;
+    // one chain per CTA: chunk m of the chain (its length and chunk count
+    // kept as values of this chain, which the loop below can see through)
+    const int Lc = (int)(ch.t1 - ch.t0);
+    const int nloop = kWrap ? nsteps : (Lc + C - 1) / C;
     auto load = [&](int m) {
       mbar_arrive_expect_tx(full, zero_v ? 3 * TILE : STAGE);
       const int row = (int)(ch.t0 + (int64_t)m * C);
-      tma_load_3d(st + 0 * TILE, &tm_q, 0, h, row, full);
-      tma_load_3d(st + 1 * TILE, &tm_k, 0, h, row, full);
-      tma_load_3d(st + 2 * TILE, &tm_th, 0, h, row, full);
-      if (!zero_v) tma_load_3d(st + 3 * TILE, &tm_v, 0, h, row, full);
+      tma_load_3d(st + 0 * TILE, &tm_q, 0, ch.head, row, full);
+      tma_load_3d(st + 1 * TILE, &tm_k, 0, ch.head, row, full);
+      tma_load_3d(st + 2 * TILE, &tm_th, 0, ch.head, row, full);
+      if (!zero_v) tma_load_3d(st + 3 * TILE, &tm_v, 0, ch.head, row, full);
     };
+    // wrapped schedule: the chunk at a cursor
+    auto load_at = [&](const Cursor& km) {
+      mbar_arrive_expect_tx(full, zero_v ? 3 * TILE : STAGE);
+      const int row = (int)km.row;
+      tma_load_3d(st + 0 * TILE, &tm_q, 0, km.head, row, full);
+      tma_load_3d(st + 1 * TILE, &tm_k, 0, km.head, row, full);
+      tma_load_3d(st + 2 * TILE, &tm_th, 0, km.head, row, full);
+      if (!zero_v) tma_load_3d(st + 3 * TILE, &tm_v, 0, km.head, row, full);
+    };
+    Cursor cur;  // wrapped schedule: the chunk of this warp's current step
+    if constexpr (kWrap) cur = cursor_at(sc, iw);
     int issued = 0, consumed = 0;
     int gram_issued = 0, gram_waited = 0;  // tcgen05 Gram products of this warp
     uint32_t tmem = 0;
     if constexpr (kTc) tmem = *(volatile uint32_t*)(sm + Ly::MISC + 8);
-    if (lane == 0 && iw < nchunks) {
+    if (lane == 0 && iw < nloop) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_th);
       prefetch_tmap(&tm_v);
-      load(iw);
+      if constexpr (kWrap)
+        load_at(cur);
+      else
+        load(iw);
     }
-    if (iw < nchunks) issued = 1;
+    if (iw < nloop) issued = 1;
     bool bad = false;
     const bool log_decay = args.gate == KDA_GATE_LOG_DECAY;  // theta holds g itself
     const f32x2 kL2 = f2(kLog2e, kLog2e);
@@ -464,14 +693,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const f32x2 kC1 = f2(args.g_min * kLog2e, args.g_min * kLog2e);
     const f32x2 kOne = f2(1.0f, 1.0f);
     const f32x2 kZero = 0ull;
-    for (int n = iw; n < nchunks; n += kIntraWarps) {
+    for (int n = iw; n < nloop; n += kIntraWarps) {
       const int slot = n % Ly::kSlots;
-      const int nvalid = min(C, L - n * C);
+      int64_t crow;  // token row of the chunk's first token
+      int h, nvalid;
+      if constexpr (kWrap) {
+        crow = cur.row;
+        h = cur.head;
+        nvalid = min(C, cur.rem);
+      } else {
+        crow = ch.t0 + (int64_t)n * C;
+        h = ch.head;
+        nvalid = min(C, Lc - n * C);
+      }
       unsigned char* sl = sm + Ly::SLOTS + slot * SLOT_BYTES;
       const uint32_t sls = sbase + Ly::SLOTS + slot * SLOT_BYTES;
       // beta of the chunk (lane t holds beta_t), issued before the waits
       float beta_l = 0.0f;
-      if (lane < nvalid) beta_l = __bfloat162float(args.beta[(ch.t0 + (int64_t)n * C + lane) * H + h]);
+      if (lane < nvalid) {
+        if constexpr (kWrap)
+          beta_l = __bfloat162float(args.beta[(crow + lane) * H + h]);
+        else
+          beta_l = __bfloat162float(args.beta[(ch.t0 + (int64_t)n * C + lane) * H + h]);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(full, consumed & 1, abort, args.wait_ns))) {
         bad = true;
         break;
@@ -609,11 +853,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) KTRACE(n, 7);
       auto refill = [&]() {
-        if (n + kIntraWarps < nchunks) {
+        if (n + kIntraWarps < nloop) {
           // the stage was only read (every value loaded from it has been used
           // by now, and __syncwarp orders the lanes' reads before this point),
           // so the copy that overwrites it needs no proxy fence
-          if (lane == 0) load(n + kIntraWarps);
+          if constexpr (kWrap) {
+            // from here on the cursor is at this warp's next step
+            cur = cursor_next(sc, cur, n, kIntraWarps);
+            if (lane == 0) load_at(cur);
+          } else {
+            if (lane == 0) load(n + kIntraWarps);
+          }
           ++issued;
         }
       };
@@ -806,18 +1056,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S[m][nt][c]: S^T element (value channel 32 sw + 16 m + g + 8 (c >> 1),
     // key channel 8 nt + 2 q + (c & 1)) -- the m16n8 accumulator layout
     float S[kMT][D / 8][4];
-#pragma unroll
-    for (int m = 0; m < kMT; ++m)
-#pragma unroll
-      for (int nt = 0; nt < D / 8; ++nt)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int dv = kDvPerWarp * sw + 16 * m + g + 8 * (c >> 1), dk = 8 * nt + 2 * q + (c & 1);
-          S[m][nt][c] = init_state ? init_state[soff + (int64_t)dk * D + dv]
-                                   : (identity && dk == dv ? 1.0f : 0.0f);
-        }
     bool bad = false;
-    for (int n = 0; n < nchunks; ++n) {
+    int n = 0;  // chunk step of this CTA
+    // one piece per chain this CTA runs (the first piece runs even with no
+    // steps: an empty chain's end state is its start state)
+    for (int piece = 0; piece == 0 || n < nsteps; ++piece) {
+      const Piece pc = sched_piece<kWrap>(sc, n);
+      // the chain's states in init/final: one chain per CTA reads its offset
+      // back from shared memory here and after the piece, so that no offset
+      // stays live through the chunk loop
+      int64_t psoff;
+      float* fsp_w = nullptr;  // wrapped instantiation: the end state
+      bool to_handoff = false;
+      if constexpr (kWrap) {
+        psoff = wrap_rt ? pc.chain * D * D : soff;
+        fsp_w = final_state ? final_state + psoff : nullptr;
+        to_handoff = pc.to_handoff;
+      } else {
+        psoff = sc.soff;
+      }
+      if (kWrap && pc.from_handoff) {
+        // the start state is handed over by the next CTA, which runs this
+        // chain's first chunks: wait for this warp's flag, then read its value
+        // channels from the chain's final-state slot
+        const uint32_t* f = args.hflags + ((int)blockIdx.x + 1) * kStateWarps + sw;
+        const bool ok = lane == 0 ? wait_flag(f, args.epoch, abort, args.wait_ns) : true;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          bad = true;
+          break;
+        }
+        __syncwarp();
+        if (ld_acquire_u32(f) != args.epoch) {
+          bad = true;
+          break;
+        }
+#pragma unroll
+        for (int m = 0; m < kMT; ++m)
+#pragma unroll
+          for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int dv = kDvPerWarp * sw + 16 * m + g + 8 * (c >> 1), dk = 8 * nt + 2 * q + (c & 1);
+              S[m][nt][c] = __ldcg(final_state + psoff + (int64_t)dk * D + dv);
+            }
+      } else {
+#pragma unroll
+        for (int m = 0; m < kMT; ++m)
+#pragma unroll
+          for (int nt = 0; nt < D / 8; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int dv = kDvPerWarp * sw + 16 * m + g + 8 * (c >> 1), dk = 8 * nt + 2 * q + (c & 1);
+              S[m][nt][c] = init_state ? init_state[psoff + (int64_t)dk * D + dv]
+                                       : (identity && dk == dv ? 1.0f : 0.0f);
+            }
+      }
+    const int pend = n + pc.steps;
+    // running over the piece's chunks: the chain's tokens from this chunk on,
+    // and the element offset of this chunk's first output row (this lane's
+    // first value channel)
+    int rem = pc.len - pc.nc0 * C;
+    int64_t rowbase = ((pc.row + (int64_t)pc.nc0 * C) * H + pc.head) * D + kDvPerWarp * sw + g;
+    for (; n < pend; ++n, rem -= C, rowbase += (int64_t)C * H * D) {
       const int slot = n % Ly::kSlots;
       const unsigned char* sl = sm + Ly::SLOTS + slot * SLOT_BYTES;
       const uint32_t sls = sbase + Ly::SLOTS + slot * SLOT_BYTES;
@@ -928,7 +1228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma16816(S[m][2 * p + 1], uh[m], b[2], b[3]);
         }
       }
-      if (n + 1 == nchunks) {
+      if (rem <= C) {  // the chain's last chunk
 #pragma unroll
         for (int p = 0; p < D / 16; ++p) {
           uint32_t b[4];
@@ -947,8 +1247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const float* dc = (const float*)(sl + SL_DC);
         const float2 dc0 = *(const float2*)(dc + 2 * q), dc1 = *(const float2*)(dc + 8 + 2 * q);
-        const int nvalid = (*sflags & kJobNoOut) ? 0 : min(C, L - n * C);
-        const int64_t row0 = ch.t0 + (int64_t)n * C;
+        const int nvalid = (*sflags & kJobNoOut) ? 0 : min(C, rem);
         {
         // the four token rows this lane writes (j, c & 1), as element offsets of
         // its first channel; the channels then differ by constants
@@ -957,7 +1256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 2; ++j)
 #pragma unroll
           for (int e = 0; e < 2; ++e)
-            rowoff[j][e] = ((row0 + 8 * j + 2 * q + e) * H + h) * D + kDvPerWarp * sw + g;
+            rowoff[j][e] = rowbase + (int64_t)((8 * j + 2 * q + e) * H) * D;
 #pragma unroll
         for (int m = 0; m < kMT; ++m)
 #pragma unroll
@@ -982,24 +1281,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[Ly::B_FREE + slot]);
       if (tid == 0) KTRACE(n, 4);
     }
-    if (bad) fail(abort, args.status);
-    if (!bad && final_state) {
+      if (bad) break;
+      float* const fsp =
+          kWrap ? fsp_w : (final_state ? final_state + (int64_t)sc.soff : nullptr);  // end state
+      if (fsp) {
+        // the end state: the chain's final state, or the hand-over of its
+        // first chunks' state to the previous CTA (through the same slot)
 #pragma unroll
-      for (int m = 0; m < kMT; ++m)
+        for (int m = 0; m < kMT; ++m)
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt)
+          for (int nt = 0; nt < D / 8; ++nt)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int dv = kDvPerWarp * sw + 16 * m + g + 8 * (c >> 1), dk = 8 * nt + 2 * q + (c & 1);
-            final_state[soff + (int64_t)dk * D + dv] = S[m][nt][c];
-          }
+            for (int c = 0; c < 4; ++c) {
+              const int dv = kDvPerWarp * sw + 16 * m + g + 8 * (c >> 1), dk = 8 * nt + 2 * q + (c & 1);
+              fsp[(int64_t)dk * D + dv] = S[m][nt][c];
+            }
+        if (to_handoff) {
+          __threadfence();  // this lane's part of the state, before the flag
+          __syncwarp();
+          if (lane == 0) st_release_u32(args.hflags + (int)blockIdx.x * kStateWarps + sw, args.epoch);
+        }
+      }
     }
+    if (bad) fail(abort, args.status);
   }
 }
 
 constexpr int kMaxAttrDevices = 64;
 std::once_flag g_attr_once[kMaxAttrDevices];
 cudaError_t g_attr_err[kMaxAttrDevices];
+// The kernel's instantiations, indexed by f = out_bf16 + 2 fallback + 4 tc_gram
+// (one chain or job per CTA, f < 8) or 8 + out_bf16 + 2 fallback (wrapped
+// schedule, mma.sync intra products).
+constexpr int kInstances = 12;
+const void* instance(int f) {
+  static const void* const fns[kInstances] = {
+      (const void*)kda_fwd_mma_kernel<false, false, false, false>,
+      (const void*)kda_fwd_mma_kernel<true, false, false, false>,
+      (const void*)kda_fwd_mma_kernel<false, true, false, false>,
+      (const void*)kda_fwd_mma_kernel<true, true, false, false>,
+      (const void*)kda_fwd_mma_kernel<false, false, true, false>,
+      (const void*)kda_fwd_mma_kernel<true, false, true, false>,
+      (const void*)kda_fwd_mma_kernel<false, true, true, false>,
+      (const void*)kda_fwd_mma_kernel<true, true, true, false>,
+      (const void*)kda_fwd_mma_kernel<false, false, false, true>,
+      (const void*)kda_fwd_mma_kernel<true, false, false, true>,
+      (const void*)kda_fwd_mma_kernel<false, true, false, true>,
+      (const void*)kda_fwd_mma_kernel<true, true, false, true>};
+  return fns[f];
+}
+size_t instance_smem(int f) { return (f >= 4 && f < 8) ? Lay<true>::BYTES : Lay<false>::BYTES; }
+
+// per device: CTAs of each instantiation that can be resident at once (0: no
+// cooperative launch, so no wrapped schedule)
+int g_coresident[kMaxAttrDevices][kInstances];
+
+// Hand-over flags of the wrapped schedule: a ring of regions, one region per
+// launch (chosen by the launch's epoch), so that launches in flight at the
+// same time on one device use distinct flags unless kHandoffRing of them
+// overlap.  A flag holds the epoch of the launch that set it last; launches
+// count their epochs from 1, so the zero-initialised array holds none.
+constexpr int kHandoffRing = 64;
+constexpr int kMaxHandoffCtas = 512;
+__device__ uint32_t g_fwd_handoff[kHandoffRing][(kMaxHandoffCtas + 1) * kStateWarps];
+std::atomic<uint32_t> g_epoch{0};
 
 }  // namespace
 
@@ -1027,19 +1372,23 @@ int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStrea
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxAttrDevices) return KDA_ERR_CUDA;
   std::call_once(g_attr_once[dev], [dev]() {
     cudaError_t err = cudaSuccess;
-    const void* fns[8] = {(const void*)kda_fwd_mma_kernel<false, false, false>,
-                          (const void*)kda_fwd_mma_kernel<true, false, false>,
-                          (const void*)kda_fwd_mma_kernel<false, true, false>,
-                          (const void*)kda_fwd_mma_kernel<true, true, false>,
-                          (const void*)kda_fwd_mma_kernel<false, false, true>,
-                          (const void*)kda_fwd_mma_kernel<true, false, true>,
-                          (const void*)kda_fwd_mma_kernel<false, true, true>,
-                          (const void*)kda_fwd_mma_kernel<true, true, true>};
-    for (int f = 0; f < 8; ++f) {
-      const void* fn = fns[f];
-      const int bytes = (int)(f < 4 ? Lay<false>::BYTES : Lay<true>::BYTES);
+    for (int f = 0; f < kInstances; ++f) {
+      const void* fn = instance(f);
+      const int bytes = (int)instance_smem(f);
       if (err == cudaSuccess)
         err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      g_coresident[dev][f] = 0;
+      if (err == cudaSuccess) {
+        int coop = 0, nsm = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, (size_t)bytes) ==
+                cudaSuccess) {
+          if (coop) g_coresident[dev][f] = nsm * per_sm;
+        } else {
+          cudaGetLastError();  // a failed query only turns the wrapped schedule off
+        }
+      }
       if (kStateRegs > 0 && err == cudaSuccess) {
         // setmaxnreg.inc can only draw on the registers the block was launched
         // with: a split above the compiled launch allocation would wait forever
@@ -1069,31 +1418,54 @@ int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStrea
   a.status = status_word_device_ptr();
   a.wait_ns = wait_ns ? wait_ns : kWaitNs;
   if (!a.status) return KDA_ERR_CUDA;
-  const unsigned grid = jobs ? (unsigned)njobs : (unsigned)(p.N * p.H);
+  unsigned grid = jobs ? (unsigned)njobs : (unsigned)(p.N * p.H);
   if (grid == 0) return KDA_OK;
   const bool fb = p.gate == KDA_GATE_LOG_DECAY;
-  if (tc_gram) {
-    constexpr uint32_t sm = Lay<true>::BYTES;
-    if (a.out_bf16 && fb)
-      kda_fwd_mma_kernel<true, true, true><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
-    else if (a.out_bf16)
-      kda_fwd_mma_kernel<true, false, true><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
-    else if (fb)
-      kda_fwd_mma_kernel<false, true, true><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
-    else
-      kda_fwd_mma_kernel<false, false, true><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
-  } else {
-    constexpr uint32_t sm = Lay<false>::BYTES;
-    if (a.out_bf16 && fb)
-      kda_fwd_mma_kernel<true, true, false><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
-    else if (a.out_bf16)
-      kda_fwd_mma_kernel<true, false, false><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
-    else if (fb)
-      kda_fwd_mma_kernel<false, true, false><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
-    else
-      kda_fwd_mma_kernel<false, false, false><<<grid, kThreads, sm, stream>>>(mq, mk, mth, mv, a);
+  // the instantiation (see instance())
+  int f = (a.out_bf16 ? 1 : 0) + (fb ? 2 : 0) + (tc_gram ? 4 : 0);
+  // Wrapped schedule: a fixed-length batch with more chains than CTAs that can
+  // be resident at once (and not a multiple of that count) would leave SMs idle
+  // in its last wave; instead, `resident` CTAs share the chains' chunks evenly
+  // (the cut chains hand their state over through their final-state slots, so
+  // the caller's final_state is needed).  All CTAs wait on one another's
+  // flags, so they are launched cooperatively (all resident at once).  The
+  // schedule is compiled for the mma.sync intra products only.
+  bool wrap = false;
+  a.wrap_cap = 0;
+  a.epoch = 0;
+  a.hflags = nullptr;
+  const int fw = 8 + (a.out_bf16 ? 1 : 0) + (fb ? 2 : 0);
+  const int resident = g_coresident[dev][fw];
+  if (!jobs && !tc_gram && !p.cu_seqlens && p.final_state && resident > 0) {
+    const int64_t chains = (int64_t)p.N * p.H;
+    const int64_t pch = ((int64_t)p.T + C - 1) / C;
+    const int64_t total = chains * pch;
+    if (chains > resident && chains % resident != 0 && total < INT32_MAX) {
+      const int64_t cap = (total + resident - 1) / resident;  // > pch: chains > resident
+      const int64_t wgrid = (total + cap - 1) / cap;
+      void* base = nullptr;
+      if (wgrid <= kMaxHandoffCtas && cudaGetSymbolAddress(&base, g_fwd_handoff) == cudaSuccess) {
+        uint32_t e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+        if (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+        wrap = true;
+        f = fw;
+        a.wrap_cap = (int)cap;
+        a.epoch = e;
+        a.hflags = (uint32_t*)base + (size_t)(e % kHandoffRing) * (kMaxHandoffCtas + 1) * kStateWarps;
+        grid = (unsigned)wgrid;
+      }
+    }
   }
-  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
+  void* kargs[5] = {(void*)&mq, (void*)&mk, (void*)&mth, (void*)&mv, (void*)&a};
+  const size_t smem = instance_smem(f);
+  const cudaError_t le =
+      wrap ? cudaLaunchCooperativeKernel(instance(f), dim3(grid), dim3(kThreads), kargs, smem, stream)
+           : cudaLaunchKernel(instance(f), dim3(grid), dim3(kThreads), kargs, smem, stream);
+  if (le != cudaSuccess) {
+    cudaGetLastError();
+    return KDA_ERR_LAUNCH;
+  }
+  return KDA_OK;
 }
 
 int launch_mma(const FwdParams& p, cudaStream_t stream, bool tc_gram) {

@@ -80,8 +80,11 @@ def _sampled(w, path, chains, seed=None):
     return inp, o, S
 
 
-# launch ranks (block index = sequence * H + head) spread over the first wave
-# (ranks 0..151 on 152 SMs) and the second (152..255)
+# chains (index = sequence * H + head) spread over the 256: under the wrapped
+# schedule (152 windows of 863 chunk-steps) chains 37, 75, 151, 170, 230 and
+# 247 are cut by a window boundary and hand their state from one CTA to
+# another, the others run whole; in a one-chain-per-CTA launch they fall in the
+# first wave (0..151) and the second (152..255)
 TRAIN_RANKS = [0, 37, 75, 118, 151, 152, 170, 199, 213, 230, 247, 255]
 
 
