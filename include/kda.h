@@ -63,8 +63,26 @@
  * Threads: every entry point may be called from several host threads at
  * once.  The only state the library keeps is per device and written once:
  * the device check, the kernels' shared-memory attributes, the status-word
- * and scratch-area addresses.  Calls that share an output buffer, a
- * workspace or the no-alloc scratch area must not overlap.
+ * and scratch-area addresses; and a launch counter of the wrapped schedule
+ * (below).  Calls that share an output buffer, a workspace or the no-alloc
+ * scratch area must not overlap.
+ *
+ * Wrapped schedule: a register-resident forward call (KDA_PATH_MMA, the AUTO
+ * choice for bf16 at dk = dv = 128) on a fixed-length batch with more
+ * (sequence, head) chains than CTAs that can be resident on the device at
+ * once (and not a multiple of that number), with final_state != NULL, runs
+ * as equal windows of 16-token chunk steps, one per resident CTA, over the
+ * chains laid end to end: no SM idles in a last, partial wave.  A chain cut
+ * by a window boundary runs its first chunks in one CTA and the rest in
+ * another; its fp32 state passes between them through the chain's own
+ * final_state slot (overwritten with the true final state at the end) and a
+ * flag in static device memory, so the results equal those of one chain
+ * per CTA bit for bit.  The launch is cooperative (every CTA resident).  The
+ * flags sit in a ring of 64 per-launch regions: up to 64 such calls may be
+ * in flight on one device at once; beyond that, overlapping calls may wait
+ * for each other's flags until their bounded wait runs out
+ * (KDA_ERR_DEVICE_TIMEOUT).  init_state and final_state may be the same
+ * buffer.  Without final_state the call runs one chain per CTA.
  */
 #ifndef KDA_H_
 #define KDA_H_

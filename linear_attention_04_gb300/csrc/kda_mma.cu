@@ -43,12 +43,21 @@
 // The diagonal of Qt Kh^T is q_t . k_t exactly (the decay factors cancel), so
 // it is taken in fp32 from the bf16 inputs and applied to U in fp32.
 //
-// A CTA runs either one whole (sequence, head) chain or, in a segmented
-// launch, one job of a table (token range, head, initial and final state, and
-// options: v taken as zero, no outputs, identity initial state), which is how
-// the segment-parallel forward obtains each segment's linear part and local
-// state.  The gate is g_min * sigmoid(theta), or theta itself as a given
-// log-decay.
+// A CTA runs one whole (sequence, head) chain; or, in a segmented launch, one
+// job of a table (token range, head, initial and final state, and options: v
+// taken as zero, no outputs, identity initial state), which is how the
+// segment-parallel forward obtains each segment's linear part and local
+// state; or, in the wrapped schedule, one equal window of chunk steps over the
+// chains laid end to end.  The wrapped schedule serves fixed-length batches
+// with more chains than CTAs that can be resident at once: one chain per CTA
+// would leave SMs idle in the last wave (256 chains on 152 SMs take two full
+// chain times), while equal windows of ceil(chains * chunks / CTAs) steps
+// (McNaughton's wrap-around rule) take 1.68.  A chain cut by a window boundary
+// runs its first chunks at the start of the later window and the rest at the
+// end of the earlier one; the fp32 state is handed over exactly, through the
+// chain's final-state slot and a release/acquire flag per state warp.  The
+// CTAs are launched cooperatively (all resident), and every wait is bounded.
+// The gate is g_min * sigmoid(theta), or theta itself as a given log-decay.
 //
 // Every wait is bounded: a wait that runs out sets the CTA's abort flag and the
 // device status word (KDA_ERR_DEVICE_TIMEOUT); every role then leaves its loop
