@@ -565,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float* init_state = args.init_state;
   float* final_state = args.final_state;
   int64_t soff = 0;  // element offset of this chain's state in init/final
-  if (args.jobs) {
+  if (!kWrap && args.jobs) {
     const SegJob jb = args.jobs[blockIdx.x];
     ch.seq = 0;
     ch.head = jb.head;
@@ -656,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* kh = sm + Ly::KH + iw * TILE;
     float* ab = (float*)(sm + Ly::AB + iw * AB_BYTES);
     uint64_t* full = &bars[Ly::B_FULL + iw];
-    const bool zero_v = *sflags & kJobZeroV;
+    const bool zero_v = !kWrap && (*sflags & kJobZeroV);
     // one chain per CTA: chunk m of the chain (its length and chunk count
     // kept as values of this chain, which the loop below can see through)
     const int Lc = (int)(ch.t1 - ch.t0);
@@ -1037,7 +1037,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       // (a test job can withhold its first hand-off: the state warps' bounded
       // wait then runs out and reports KDA_ERR_DEVICE_TIMEOUT)
-      if (lane == 0 && !(n == 0 && (*sflags & kJobTestWithholdFirst))) {
+      if (lane == 0 && !(!kWrap && n == 0 && (*sflags & kJobTestWithholdFirst))) {
         mbar_arrive(&bars[Ly::B_READY + slot]);
         KTRACE(n, 10);
       }
@@ -1061,7 +1061,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ state warps
     if constexpr (kStateRegs > 0) set_regs<kStateRegs>();
     const int sw = warp;
-    const bool identity = flags & kJobIdentityInit;
+    const bool identity = !kWrap && (flags & kJobIdentityInit);
     // S[m][nt][c]: S^T element (value channel 32 sw + 16 m + g + 8 (c >> 1),
     // key channel 8 nt + 2 q + (c & 1)) -- the m16n8 accumulator layout
     float S[kMT][D / 8][4];
@@ -1256,7 +1256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const float* dc = (const float*)(sl + SL_DC);
         const float2 dc0 = *(const float2*)(dc + 2 * q), dc1 = *(const float2*)(dc + 8 + 2 * q);
-        const int nvalid = (*sflags & kJobNoOut) ? 0 : min(C, rem);
+        const int nvalid = (!kWrap && (*sflags & kJobNoOut)) ? 0 : min(C, rem);
         {
         // the four token rows this lane writes (j, c & 1), as element offsets of
         // its first channel; the channels then differ by constants

@@ -145,3 +145,26 @@ def test_wrapped_in_place_state():
     tol = TOL[torch.bfloat16]
     assert_close(f64(o), ro, tol, "in-place out")
     assert_close(f64(S), rS, tol, "in-place state")
+
+
+def test_wrapped_flag_ring_reuse():
+    # 140 wrapped launches in a row: each flag region of the 64-slot ring is
+    # reused with the flags of an older launch still in it; a flag only passes
+    # when it holds the current launch's epoch, so every launch must give the
+    # same outputs and final states, bit for bit
+    B, H = _batch(8, 16)
+    w = Workload("wrap", B=B, H=H, T=48, dk=128, dv=128, dtype=torch.bfloat16, init_std=0.02)
+    c = _cuda(make_inputs(w, seed=46))
+    o0, S0 = _fwd(c, c["theta"], "mma", "sigmoid")
+    out = torch.empty_like(o0)
+    S = torch.empty_like(S0)
+    for i in range(140):
+        kda_chunk_fwd(c["q"], c["k"], c["v"], c["theta"], c["beta"], -5.0, c["init_state"], out, S,
+                      path="mma")
+        if i % 20 == 19:
+            torch.cuda.synchronize()
+            assert kda_device_status(clear=True) == 0
+            assert torch.equal(out, o0) and torch.equal(S, S0), f"launch {i}"
+    torch.cuda.synchronize()
+    assert kda_device_status(clear=True) == 0
+    assert torch.equal(out, o0) and torch.equal(S, S0)
