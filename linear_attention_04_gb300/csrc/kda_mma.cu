@@ -533,15 +533,21 @@ __device__ __forceinline__ void fail(volatile int* abort, int* status) {
 // kFallback: compile the position-wise fallback for chunks whose decay is too
 // steep for the dense tile (only a given, unbounded log-decay can produce
 // them; the bounded gate's kernel carries no such code)
-// kWrap: the wrapped schedule (one window of chunk steps per CTA); otherwise
-// one chain (or one segment job) per CTA.
-template <bool kOutBf16, bool kFallback, bool kTc, bool kWrap>
+// The CTA's work unit (template parameter kMode): one whole chain
+// (kModeChain), one job of a table (kModeJobs, the segmented forward and the
+// failure-test hook: the job options are compiled in only here), or one
+// window of the wrapped schedule (kModeWrap).
+constexpr int kModeChain = 0, kModeJobs = 1, kModeWrap = 2;
+
+template <bool kOutBf16, bool kFallback, bool kTc, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_fwd_mma_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_th,
                        const __grid_constant__ CUtensorMap tm_v, const MmaArgs args) {
   using Ly = Lay<kTc>;
+  constexpr bool kWrap = kMode == kModeWrap;
+  constexpr bool kJobs = kMode == kModeJobs;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // pointer arithmetic on the shared array itself keeps the shared address
   // space visible to the compiler (32-bit shared addressing); the swizzled
@@ -565,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float* init_state = args.init_state;
   float* final_state = args.final_state;
   int64_t soff = 0;  // element offset of this chain's state in init/final
-  if (!kWrap && args.jobs) {
+  if (kJobs) {
     const SegJob jb = args.jobs[blockIdx.x];
     ch.seq = 0;
     ch.head = jb.head;
@@ -656,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* kh = sm + Ly::KH + iw * TILE;
     float* ab = (float*)(sm + Ly::AB + iw * AB_BYTES);
     uint64_t* full = &bars[Ly::B_FULL + iw];
-    const bool zero_v = !kWrap && (*sflags & kJobZeroV);
+    const bool zero_v = kJobs && (*sflags & kJobZeroV);
     // one chain per CTA: chunk m of the chain (its length and chunk count
     // kept as values of this chain, which the loop below can see through)
     const int Lc = (int)(ch.t1 - ch.t0);
@@ -1037,7 +1043,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       // (a test job can withhold its first hand-off: the state warps' bounded
       // wait then runs out and reports KDA_ERR_DEVICE_TIMEOUT)
-      if (lane == 0 && !(!kWrap && n == 0 && (*sflags & kJobTestWithholdFirst))) {
+      if (lane == 0 && !(kJobs && n == 0 && (*sflags & kJobTestWithholdFirst))) {
         mbar_arrive(&bars[Ly::B_READY + slot]);
         KTRACE(n, 10);
       }
@@ -1061,7 +1067,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ state warps
     if constexpr (kStateRegs > 0) set_regs<kStateRegs>();
     const int sw = warp;
-    const bool identity = !kWrap && (flags & kJobIdentityInit);
+    const bool identity = kJobs && (flags & kJobIdentityInit);
     // S[m][nt][c]: S^T element (value channel 32 sw + 16 m + g + 8 (c >> 1),
     // key channel 8 nt + 2 q + (c & 1)) -- the m16n8 accumulator layout
     float S[kMT][D / 8][4];
@@ -1256,7 +1262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const float* dc = (const float*)(sl + SL_DC);
         const float2 dc0 = *(const float2*)(dc + 2 * q), dc1 = *(const float2*)(dc + 8 + 2 * q);
-        const int nvalid = (!kWrap && (*sflags & kJobNoOut)) ? 0 : min(C, rem);
+        const int nvalid = (kJobs && (*sflags & kJobNoOut)) ? 0 : min(C, rem);
         {
         // the four token rows this lane writes (j, c & 1), as element offsets of
         // its first channel; the channels then differ by constants
@@ -1320,26 +1326,35 @@ constexpr int kMaxAttrDevices = 64;
 std::once_flag g_attr_once[kMaxAttrDevices];
 cudaError_t g_attr_err[kMaxAttrDevices];
 // The kernel's instantiations, indexed by f = out_bf16 + 2 fallback + 4 tc_gram
-// (one chain or job per CTA, f < 8) or 8 + out_bf16 + 2 fallback (wrapped
-// schedule, mma.sync intra products).
-constexpr int kInstances = 12;
+// (one chain per CTA: f < 8; one job per CTA: 8 + that) or 16 + out_bf16 +
+// 2 fallback (wrapped schedule, mma.sync intra products).
+constexpr int kInstances = 20;
+template <int kMode>
+constexpr void fill_instances(const void** fns) {
+  fns[0] = (const void*)kda_fwd_mma_kernel<false, false, false, kMode>;
+  fns[1] = (const void*)kda_fwd_mma_kernel<true, false, false, kMode>;
+  fns[2] = (const void*)kda_fwd_mma_kernel<false, true, false, kMode>;
+  fns[3] = (const void*)kda_fwd_mma_kernel<true, true, false, kMode>;
+  if constexpr (kMode != kModeWrap) {
+    fns[4] = (const void*)kda_fwd_mma_kernel<false, false, true, kMode>;
+    fns[5] = (const void*)kda_fwd_mma_kernel<true, false, true, kMode>;
+    fns[6] = (const void*)kda_fwd_mma_kernel<false, true, true, kMode>;
+    fns[7] = (const void*)kda_fwd_mma_kernel<true, true, true, kMode>;
+  }
+}
 const void* instance(int f) {
-  static const void* const fns[kInstances] = {
-      (const void*)kda_fwd_mma_kernel<false, false, false, false>,
-      (const void*)kda_fwd_mma_kernel<true, false, false, false>,
-      (const void*)kda_fwd_mma_kernel<false, true, false, false>,
-      (const void*)kda_fwd_mma_kernel<true, true, false, false>,
-      (const void*)kda_fwd_mma_kernel<false, false, true, false>,
-      (const void*)kda_fwd_mma_kernel<true, false, true, false>,
-      (const void*)kda_fwd_mma_kernel<false, true, true, false>,
-      (const void*)kda_fwd_mma_kernel<true, true, true, false>,
-      (const void*)kda_fwd_mma_kernel<false, false, false, true>,
-      (const void*)kda_fwd_mma_kernel<true, false, false, true>,
-      (const void*)kda_fwd_mma_kernel<false, true, false, true>,
-      (const void*)kda_fwd_mma_kernel<true, true, false, true>};
+  static const void* fns[kInstances] = {};
+  static std::once_flag once;
+  std::call_once(once, []() {
+    fill_instances<kModeChain>(fns);
+    fill_instances<kModeJobs>(fns + 8);
+    fill_instances<kModeWrap>(fns + 16);
+  });
   return fns[f];
 }
-size_t instance_smem(int f) { return (f >= 4 && f < 8) ? Lay<true>::BYTES : Lay<false>::BYTES; }
+size_t instance_smem(int f) {
+  return (f < 16 && (f & 4)) ? Lay<true>::BYTES : Lay<false>::BYTES;
+}
 
 // per device: CTAs of each instantiation that can be resident at once (0: no
 // cooperative launch, so no wrapped schedule)
@@ -1431,7 +1446,7 @@ int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStrea
   if (grid == 0) return KDA_OK;
   const bool fb = p.gate == KDA_GATE_LOG_DECAY;
   // the instantiation (see instance())
-  int f = (a.out_bf16 ? 1 : 0) + (fb ? 2 : 0) + (tc_gram ? 4 : 0);
+  int f = (a.out_bf16 ? 1 : 0) + (fb ? 2 : 0) + (tc_gram ? 4 : 0) + (jobs ? 8 : 0);
   // Wrapped schedule: a fixed-length batch with more chains than CTAs that can
   // be resident at once (and not a multiple of that count) would leave SMs idle
   // in its last wave; instead, `resident` CTAs share the chains' chunks evenly
@@ -1443,7 +1458,7 @@ int launch_mma_jobs(const FwdParams& p, const SegJob* jobs, int njobs, cudaStrea
   a.wrap_cap = 0;
   a.epoch = 0;
   a.hflags = nullptr;
-  const int fw = 8 + (a.out_bf16 ? 1 : 0) + (fb ? 2 : 0);
+  const int fw = 16 + (a.out_bf16 ? 1 : 0) + (fb ? 2 : 0);
   const int resident = g_coresident[dev][fw];
   if (!jobs && !tc_gram && !p.cu_seqlens && p.final_state && resident > 0) {
     const int64_t chains = (int64_t)p.N * p.H;
