@@ -639,8 +639,8 @@ def bwd_bytes(w, inp, e=2) -> int:
     return n * (e * (3 * w.dk + w.dv) + e + 4 * w.dv + 4 * (3 * w.dk + w.dv) + 4)
 
 
-# kda_chunk_bwd launches the recurrences kernel, then the gradient kernel
-BWD_LAUNCHES_PER_PASS = 2
+# kda_chunk_bwd clears its work queue and launches one persistent kernel
+BWD_LAUNCHES_PER_PASS = 1
 
 
 def run_bwd(args, rank, world, local):
@@ -697,7 +697,7 @@ def run_bwd(args, rank, world, local):
                          "frac": round(achieved / FP32_ALU_TFLOPS, 4), "traffic": traffic,
                          "traffic_source": traffic_src,
                          "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 x 2070 MHz",
-                         "kernel": "kda_bwd_recurrences_kernel + kda_bwd_grads_kernel (one pass)",
+                         "kernel": "kda_bwd_kernel (one persistent launch per pass)",
                          "algorithmic_flops_per_pass": flops,
                          "hbm": {"achieved_gbs": round(nbytes / step_s / 1e9, 1),
                                  "peak_gbs": peaks["hbm_gbs"],

@@ -79,6 +79,10 @@ struct BwdDev {
   float* ws_dS;  // [chain][chunk][128][128] gradient w.r.t. each chunk's end state
   float* ws_dU;  // [chain][chunk][16][128]
   float* ws_RU;  // [chain][chunk][2][16][128]: R = V - Kt S and U = Tb R of each chunk
+  unsigned long long* q_next;  // work-queue position (zeroed before the launch)
+  int* q_done;                 // [chain] recurrences of the chain finished (0, 1 or 2)
+  int* status;                 // device status word
+  uint64_t wait_ns;            // limit of a gradient item's wait for its chain
   int H, T, nch;
 };
 
@@ -1053,23 +1057,21 @@ __device__ __forceinline__ void reverse_chain(const BwdDev& a, int64_t chain) {
   if (a.d_init) group_state_store(st, a.d_init + chain * kStateF, D, gt);
 }
 
-// The two recurrences are independent of each other and run as one grid: CTAs
-// 0 .. chains-1 run the reverse recurrence (the longer one per chunk) and CTAs
-// chains .. 2 chains-1 the forward one, so that the two sets of chains share
-// the SMs without a wave boundary between them.
+// The two recurrences of every chain are independent of each other: items
+// 0 .. chains-1 of the work queue run the reverse recurrence (the longer one
+// per chunk), items chains .. 2 chains-1 the forward one.
 template <typename Tin>
-__global__ void __launch_bounds__(kThreads, 1) kda_bwd_recurrences_kernel(const BwdDev a,
-                                                                          int64_t chains) {
-  const int64_t blk = blockIdx.x;
-  if (blk < chains)
-    reverse_chain<Tin>(a, blk);
+__device__ __forceinline__ void recurrence_item(const BwdDev& a, int64_t chains, int64_t item) {
+  if (item < chains)
+    reverse_chain<Tin>(a, item);
   else
-    states_chain<Tin>(a, blk - chains);
+    states_chain<Tin>(a, item - chains);
 }
 
 // ------------------------------------------------------ per-chunk gradients
+// Every gradient of chunk n of one chain, item = chain * nch + n.
 template <typename Tin>
-__global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev a) {
+__device__ __forceinline__ void grads_chunk(const BwdDev& a, int64_t item) {
   extern __shared__ __align__(16) float smf[];
   float* S = smf;  // S, then dS'
   float* Qt = S + STATE_F;
@@ -1101,8 +1103,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
   float* dbt = bt + C;
   float* dpd = dbt + C;  // diagonal of dPi
   const int tid = threadIdx.x, ig = tid >> 4, jg = tid & 15;
-  const int64_t chain = blockIdx.x / a.nch;
-  const int n = (int)(blockIdx.x - chain * a.nch);
+  const int64_t chain = item / a.nch;
+  const int n = (int)(item - chain * a.nch);
   const int64_t b = chain / a.H;
   const int h = (int)(chain - b * a.H);
   const int t0 = n * C, nvalid = min(C, a.T - t0);
@@ -1329,6 +1331,72 @@ __global__ void __launch_bounds__(kThreads, 1) kda_bwd_grads_kernel(const BwdDev
   if (tid < nvalid) a.dbeta[(row0 + tid) * a.H + h] = dbt[tid];
 }
 
+// Bytes of the work queue at the end of the workspace: the queue position
+// (256 bytes, for alignment), then one int per chain, rounded up to 256 bytes.
+constexpr size_t queue_bytes(int64_t chains) {
+  return 256 + ((size_t)chains * sizeof(int) + 255) / 256 * 256;
+}
+
+// Waits until *f >= want (acquire); gives up after limit_ns.
+__device__ __forceinline__ bool wait_count(const int* f, int want, uint64_t limit_ns) {
+  auto ld = [](const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+  };
+  if (ld(f) >= want) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (;;) {
+    __nanosleep(1000);
+    if (ld(f) >= want) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > limit_ns) return false;
+  }
+}
+
+// The whole backward pass as one persistent launch over a work queue (one CTA
+// per SM).  A CTA takes the next item from a counter in the workspace: first
+// the 2 chains recurrences (reverse ones first: the longest first), then the
+// chains * nch per-chunk gradient items, chain by chain.  A gradient item
+// needs both recurrences of its chain: it waits for the chain's count of
+// finished recurrences to reach 2.  Every recurrence item is taken before any
+// gradient item, and only by a running CTA, so the waits always end; meanwhile
+// the SMs that the recurrences' last wave leaves idle already run the
+// gradients of the chains that are done (a separate gradient launch would
+// start only after the last recurrence).  A wait that runs out (bounded by
+// wait_ns) records KDA_ERR_DEVICE_TIMEOUT and skips the item.
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads, 1) kda_bwd_kernel(const BwdDev a, int64_t chains) {
+  __shared__ long long s_item;
+  __shared__ int s_ok;
+  const int64_t items = 2 * chains + chains * a.nch;
+  for (;;) {
+    if (threadIdx.x == 0) s_item = (long long)atomicAdd(a.q_next, 1ull);
+    __syncthreads();
+    const int64_t item = s_item;
+    if (item >= items) break;
+    if (item < 2 * chains) {
+      recurrence_item<Tin>(a, chains, item);
+      cp_async_wait_all();
+      __threadfence();  // this thread's workspace writes, before the count
+      __syncthreads();
+      if (threadIdx.x == 0) atomicAdd(a.q_done + (item < chains ? item : item - chains), 1);
+    } else {
+      const int64_t g = item - 2 * chains;
+      if (threadIdx.x == 0) {
+        s_ok = wait_count(a.q_done + g / a.nch, 2, a.wait_ns);
+        if (!s_ok) atomicExch(a.status, KDA_ERR_DEVICE_TIMEOUT);
+      }
+      __syncthreads();
+      if (s_ok) grads_chunk<Tin>(a, g);
+      cp_async_wait_all();
+    }
+    __syncthreads();  // the item's shared memory and s_item are free again
+  }
+}
+
 template <typename Tin>
 constexpr size_t smem_states() {
   return (size_t)(STATE_F + 2 * BUF_F + TILE_F + 7 * SM16_F + TILE_F + 2 * TILE_F) * 4 +
@@ -1347,16 +1415,22 @@ template <typename Tin>
 int launch_bwd_t(const BwdDev& d, int64_t chains, cudaStream_t stream) {
   constexpr size_t kSmemRec =
       smem_states<Tin>() > smem_reverse<Tin>() ? smem_states<Tin>() : smem_reverse<Tin>();
-  const void* fns[2] = {(const void*)kda_bwd_recurrences_kernel<Tin>,
-                        (const void*)kda_bwd_grads_kernel<Tin>};
-  const size_t smem[2] = {kSmemRec, kSmemGrads};
-  for (int i = 0; i < 2; ++i)
-    if (cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem[i]) !=
-        cudaSuccess)
-      return KDA_ERR_LAUNCH;
-  if (2 * chains > (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
-  kda_bwd_recurrences_kernel<Tin><<<(unsigned)(2 * chains), kThreads, kSmemRec, stream>>>(d, chains);
-  kda_bwd_grads_kernel<Tin><<<(unsigned)(chains * d.nch), kThreads, kSmemGrads, stream>>>(d);
+  constexpr size_t kSmem = kSmemRec > kSmemGrads ? kSmemRec : kSmemGrads;
+  const void* fn = (const void*)kda_bwd_kernel<Tin>;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) !=
+      cudaSuccess)
+    return KDA_ERR_LAUNCH;
+  int dev = 0, nsm = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, kSmem) != cudaSuccess ||
+      nsm <= 0 || per_sm <= 0)
+    return KDA_ERR_LAUNCH;
+  const int64_t items = 2 * chains + chains * d.nch;
+  const int64_t grid = items < (int64_t)nsm * per_sm ? items : (int64_t)nsm * per_sm;
+  // the queue position and the per-chain counts start at zero
+  if (cudaMemsetAsync(d.q_next, 0, queue_bytes(chains), stream) != cudaSuccess) return KDA_ERR_CUDA;
+  kda_bwd_kernel<Tin><<<(unsigned)grid, kThreads, kSmem, stream>>>(d, chains);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_LAUNCH;
 }
 
@@ -1364,7 +1438,8 @@ int launch_bwd_t(const BwdDev& d, int64_t chains, cudaStream_t stream) {
 
 size_t bwd_workspace_size(int B, int H, int T) {
   const size_t nch = ((size_t)T + C - 1) / C;
-  return (size_t)B * H * nch * (2 * kStateF + (size_t)3 * C * D) * sizeof(float);
+  return (size_t)B * H * nch * (2 * kStateF + (size_t)3 * C * D) * sizeof(float) +
+         queue_bytes((int64_t)B * H);
 }
 
 // (dk = dv = 128 is checked by the caller)
@@ -1394,6 +1469,11 @@ int launch_bwd(const BwdParams& p, cudaStream_t stream) {
   d.ws_dS = d.ws_S + (size_t)chains * nch * kStateF;
   d.ws_dU = d.ws_dS + (size_t)chains * nch * kStateF;
   d.ws_RU = d.ws_dU + (size_t)chains * nch * C * D;
+  d.q_next = (unsigned long long*)(d.ws_RU + (size_t)chains * nch * 2 * C * D);
+  d.q_done = (int*)((unsigned char*)d.q_next + 256);
+  d.status = status_word_device_ptr();
+  if (!d.status) return KDA_ERR_CUDA;
+  d.wait_ns = 2000000000ull;
   d.H = p.H;
   d.T = p.T;
   d.nch = nch;

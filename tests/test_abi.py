@@ -224,9 +224,15 @@ def test_bwd_workspace_rules():
     lib = binding.load()
     # per chain and 16-token chunk: the chunk-start state, the end-of-chunk
     # state gradient (128 x 128 fp32 each), dU, R and U (16 x 128 fp32 each)
+    # per chunk: two fp32 128 x 128 states and three 16 x 128 tiles; then the
+    # work queue: its position (256 bytes) and one int per chain, in 256-byte units
+    queue = 256 + 256
     n = lib.kda_chunk_bwd_workspace_size(1, 2, 64, 128, 128)
-    assert n == 2 * 4 * (2 * 128 * 128 + 3 * 16 * 128) * 4
-    assert lib.kda_chunk_bwd_workspace_size(1, 2, 65, 128, 128) == 2 * 5 * (2 * 128 * 128 + 3 * 16 * 128) * 4
+    assert n == 2 * 4 * (2 * 128 * 128 + 3 * 16 * 128) * 4 + queue
+    assert lib.kda_chunk_bwd_workspace_size(1, 2, 65, 128, 128) == \
+        2 * 5 * (2 * 128 * 128 + 3 * 16 * 128) * 4 + queue
+    assert lib.kda_chunk_bwd_workspace_size(8, 32, 16, 128, 128) == \
+        256 * (2 * 128 * 128 + 3 * 16 * 128) * 4 + 256 + 1024
     assert lib.kda_chunk_bwd_workspace_size(1, 2, 64, 64, 128) == 0
     a = _bwd_args()
     assert lib.kda_chunk_bwd(ctypes.byref(a), 0x100000, n - 1, None) == binding.KDA_ERR_INVALID_ARG
