@@ -254,8 +254,11 @@ KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* args, int segments, void
  * gradient and d_out/d_final are fp32.  `gate` as kda_fwd_args.gate.
  * `workspace`: device memory of kda_chunk_bwd_workspace_size(B, H, T, dk, dv)
  * bytes (B * H * ceil(T / 16) * 152 KB: two fp32 128 x 128 states and three
- * 16 x 128 fp32 tiles per chunk), 16-byte aligned, caller-owned, scratch until
- * the stream has passed the call; it needs no initial contents.  The library
+ * 16 x 128 fp32 tiles per chunk; then a work queue of 256 bytes plus one int
+ * per (sequence, head) chain rounded up to 256 bytes), 16-byte aligned,
+ * caller-owned, scratch until the stream has passed the call; it needs no
+ * initial contents (the call clears the queue with a memset on `stream`
+ * before its one kernel launch).  The library
  * allocates nothing.  A given log-decay (KDA_GATE_LOG_DECAY) has the forward
  * pass's limit: the in-chunk sum of |g| below about 88.  Returns KDA_OK or
  * KDA_ERR_*.

@@ -24,13 +24,14 @@
 //   (summed as sum_{s >= t} (dG_s + dKhC_s KhC_s) + sum_{s < t} dKhC_s KhC_s + dec ec),
 //   dtheta = dg g_min sigmoid(theta) sigmoid(-theta)   (dg for a given log-decay).
 //
-// Two launches over a caller workspace:
-//   1. kda_bwd_recurrences_kernel, two CTAs per chain (independent of each
-//      other): the forward recurrence, writing the state at the start of every
-//      chunk and R, U of every chunk; and the reverse recurrence of dS, writing
-//      dS' and dU of every chunk, and dV;
-//   2. kda_bwd_grads_kernel, one CTA per chunk, all chunks in parallel: every
-//      other gradient from S, dS', dU, R, U and the chunk's inputs.
+// One persistent launch (kda_bwd_kernel) over a caller workspace, its CTAs
+// taking items from a work queue:
+//   1. two recurrences per chain (independent of each other): the forward
+//      recurrence, writing the state at the start of every chunk and R, U of
+//      every chunk; and the reverse recurrence of dS, writing dS' and dU of
+//      every chunk, and dV;
+//   2. one item per chunk: every other gradient from S, dS', dU, R, U and the
+//      chunk's inputs, once both recurrences of its chain are done.
 // The recurrences carry their 128 x 128 state in registers with a copy in
 // shared memory for the products that contract over it, and stage the next
 // chunk's inputs in shared memory with cp.async while the current chunk
