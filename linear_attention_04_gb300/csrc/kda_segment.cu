@@ -24,8 +24,23 @@
 // on otherwise idle SMs.  All scratch lives in a caller-provided workspace
 // (kda_segmented_workspace_size).  Segments are whole 32-token units, the
 // state step of the tcgen05 kernel (two 16-token chunks).
+//
+// Segment 0 may be longer than the others.  Launch 1 holds segment 0 of every
+// chain and two jobs for each of segments 1 .. P-2, launch 2 one job for each
+// of segments 1 .. P-1, and each launch takes as long as its busiest SM: with
+// more jobs than SMs, the jobs after the first wave wait for SMs to free up.
+// A segment 0 of twice the others' length runs beside the first wave of the
+// short jobs of launch 1 and lets the rest of them follow on the same SMs:
+// e.g. 32 chains, P = 5, 152 SMs: equal segments take 2 + 1 waves of L/5
+// (0.6 L), a first segment of 2 L/6 takes 2 L/6 + L/6 (0.5 L).  The plan
+// picks whichever of the two splits a list-scheduling model of the launches
+// (jobs in launch order on the device's SMs) finishes first.
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <functional>
+#include <queue>
+#include <vector>
 
 #include "kda_internal.cuh"
 
@@ -39,14 +54,44 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct SegPlan {
   int P;           // segments per chain (effective)
-  int64_t Ltok;    // tokens per segment (whole chunks; the last may be shorter)
+  int64_t L0tok;   // tokens of segment 0
+  int64_t Ltok;    // tokens of segments 1 .. P-1 (whole units; the last may be shorter)
   int64_t NH;      // chains
   size_t off_jobs1, off_jobs2, off_sst, off_sloc, off_phi, total;
 };
 
 constexpr int kSegUnit = 2 * kChunk;  // tokens per segmentation unit
 
-SegPlan plan(int B, int H, int T, int segments) {
+// Time (in units) until `sms` SMs have run jobs of the given lengths, each job
+// starting on the first SM to become free, in order.
+int64_t list_schedule(const std::vector<int64_t>& jobs, int sms) {
+  std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> free_at;
+  for (int i = 0; i < sms; ++i) free_at.push(0);
+  int64_t end = 0;
+  for (int64_t len : jobs) {
+    const int64_t t = free_at.top() + len;
+    free_at.pop();
+    free_at.push(t);
+    if (t > end) end = t;
+  }
+  return end;
+}
+
+// Model of the two launches for segment 0 of u0 units and the others of u
+// units (the last one what is left of n units).
+int64_t model_time(int64_t NH, int P, int64_t n, int64_t u0, int64_t u, int sms) {
+  std::vector<int64_t> j1, j2;
+  j1.assign((size_t)NH, u0);
+  j1.insert(j1.end(), (size_t)(NH * 2 * (P - 2)), u);
+  for (int s = 1; s <= P - 1; ++s) {
+    const int64_t len = s < P - 1 ? u : n - u0 - (int64_t)(P - 2) * u;
+    j2.insert(j2.end(), (size_t)NH, len);
+  }
+  return list_schedule(j1, sms) + list_schedule(j2, sms);
+}
+
+// sms > 0: choose segment 0's length by the model above (else equal segments).
+SegPlan plan(int B, int H, int T, int segments, int sms = 0) {
   SegPlan s;
   const int64_t nchunks = ((int64_t)T + kSegUnit - 1) / kSegUnit;
   int P = segments < 1 ? 1 : segments;
@@ -54,8 +99,19 @@ SegPlan plan(int B, int H, int T, int segments) {
   const int64_t per = (nchunks + P - 1) / P;  // chunks per segment
   P = (int)((nchunks + per - 1) / per);       // no empty segment
   s.P = P;
+  s.L0tok = per * kSegUnit;
   s.Ltok = per * kSegUnit;
   s.NH = (int64_t)B * H;
+  if (sms > 0 && P >= 3 && s.NH * 3 * P <= 200000) {
+    // segment 0 twice as long as the others, if the last segment keeps some
+    // tokens and the model says it finishes first
+    const int64_t u = (nchunks + P) / (P + 1);
+    if (2 * u + (int64_t)(P - 2) * u < nchunks &&
+        model_time(s.NH, P, nchunks, 2 * u, u, sms) < model_time(s.NH, P, nchunks, per, per, sms)) {
+      s.L0tok = 2 * u * kSegUnit;
+      s.Ltok = u * kSegUnit;
+    }
+  }
   const int64_t n1 = s.NH * (P >= 2 ? 2 * P - 3 : 0);
   const int64_t n2 = s.NH * (P - 1);
   const size_t st = (size_t)D * D * sizeof(float);
@@ -71,16 +127,19 @@ SegPlan plan(int B, int H, int T, int segments) {
 // Fills both job tables (one thread per chain).
 __global__ void seg_setup_kernel(SegJob* jobs1, SegJob* jobs2, float* sst, float* sloc, float* phi,
                                  const float* init, float* fin, int64_t NH, int H, int64_t T,
-                                 int P, int64_t Ltok) {
+                                 int P, int64_t L0tok, int64_t Ltok) {
   const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= NH) return;
   const int64_t b = c / H;
   const int h = (int)(c - b * H);
   const int64_t base = b * T;
   const size_t st = (size_t)D * D;
+  // segment s: tokens [start(s), start(s + 1)), start(s) = L0tok + (s - 1) Ltok
   auto seg = [&](int s, SegJob& j) {
-    j.t0 = base + (int64_t)s * Ltok;
-    j.t1 = base + ((int64_t)(s + 1) * Ltok < T ? (int64_t)(s + 1) * Ltok : T);
+    const int64_t a = s == 0 ? 0 : L0tok + (int64_t)(s - 1) * Ltok;
+    const int64_t e = L0tok + (int64_t)s * Ltok;
+    j.t0 = base + a;
+    j.t1 = base + (e < T ? e : T);
     j.head = h;
   };
   // launch 1: segment 0 in full; segments 1 .. P-2 local and transition
@@ -148,7 +207,11 @@ int launch_segmented(const FwdParams& p, int segments, void* ws, size_t ws_bytes
     return mma ? launch_mma_jobs(q, jobs, njobs, stream)
                : launch_tc32_jobs(q, jobs, njobs, stream, 0, split_s);
   };
-  const SegPlan pl = plan(p.N, p.H, p.T, segments);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  const SegPlan pl = plan(p.N, p.H, p.T, segments, sms);
   if (pl.P < 2) return mma ? launch_mma(p, stream) : launch_tc32_jobs(p, nullptr, 0, stream, 0, split_s);
   if (!ws || ws_bytes < pl.total) return KDA_ERR_INVALID_ARG;
   unsigned char* w = (unsigned char*)ws;
@@ -158,7 +221,8 @@ int launch_segmented(const FwdParams& p, int segments, void* ws, size_t ws_bytes
   float* sloc = (float*)(w + pl.off_sloc);
   float* phi = (float*)(w + pl.off_phi);
   seg_setup_kernel<<<(unsigned)((pl.NH + 127) / 128), 128, 0, stream>>>(
-      jobs1, jobs2, sst, sloc, phi, p.init_state, p.final_state, pl.NH, p.H, p.T, pl.P, pl.Ltok);
+      jobs1, jobs2, sst, sloc, phi, p.init_state, p.final_state, pl.NH, p.H, p.T, pl.P, pl.L0tok,
+      pl.Ltok);
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
   // the kernels see the batch as one packed sequence of B * T tokens
   FwdParams q = p;

@@ -33,6 +33,23 @@ def test_segmented_vs_oracle(T, segments):
     assert_close(f64(S), ref_S, TOL_BF16, f"segmented final state T={T} P={segments}")
 
 
+@pytest.mark.parametrize("path", ["mma", "tc"])
+def test_segmented_longer_first_segment(path):
+    # 32 chains, P = 5 on 152 SMs: launch 1 holds 32 + 192 jobs, so the plan
+    # makes segment 0 twice as long as the others (it runs beside the first
+    # wave of the short jobs); every chain against the oracle
+    w = Workload("seg", B=1, H=32, T=2048, dk=128, dv=128, dtype=torch.bfloat16, init_std=0.05)
+    inp = make_inputs(w, seed=1077)
+    g = _cuda(inp)
+    ref_o, ref_S = oracle_full(inp)
+    o, S = kda_chunk_fwd_segmented(g["q"], g["k"], g["v"], g["theta"], g["beta"], -5.0,
+                                   g["init_state"], segments=5, path=path)
+    torch.cuda.synchronize()
+    assert kda_device_status(clear=True) == 0
+    assert_close(f64(o), ref_o, TOL_BF16, f"segmented out, longer first segment ({path})")
+    assert_close(f64(S), ref_S, TOL_BF16, f"segmented final state, longer first segment ({path})")
+
+
 def test_segmented_slow_channels_carry_state_across_segments():
     # 16 key channels with theta shifted by -12 (g ~ -3e-5 per token) carry the
     # state across every segment boundary, so Phi and the chaining matter; the
