@@ -1359,7 +1359,7 @@ __device__ __forceinline__ bool wait_count(const int* f, int want, uint64_t limi
 
 // The whole backward pass as one persistent launch over a work queue (one CTA
 // per SM).  A CTA takes the next item from a counter in the workspace: first
-// the 2 chains recurrences (reverse ones first: the longest first), then the
+// the 2 x chains recurrences (reverse ones first: the longest first), then the
 // chains * nch per-chunk gradient items, chain by chain.  A gradient item
 // needs both recurrences of its chain: it waits for the chain's count of
 // finished recurrences to reach 2.  Every recurrence item is taken before any
@@ -1474,7 +1474,9 @@ int launch_bwd(const BwdParams& p, cudaStream_t stream) {
   d.q_done = (int*)((unsigned char*)d.q_next + 256);
   d.status = status_word_device_ptr();
   if (!d.status) return KDA_ERR_CUDA;
-  d.wait_ns = 2000000000ull;
+  // a gradient item may wait for a whole recurrence of its chain (about 10 us
+  // per chunk): 2 s plus 50 us per chunk
+  d.wait_ns = 2000000000ull + (uint64_t)nch * 50000ull;
   d.H = p.H;
   d.T = p.T;
   d.nch = nch;
