@@ -1181,14 +1181,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* s1 = S[m][2 * kk + 1];
           const uint32_t a[4] = {pack_bf16x2(s0[0], s0[1]), pack_bf16x2(s0[2], s0[3]),
                                  pack_bf16x2(s1[0], s1[1]), pack_bf16x2(s1[2], s1[3])};
-          s0[0] *= e0.x;
-          s0[1] *= e0.y;
-          s0[2] *= e0.x;
-          s0[3] *= e0.y;
-          s1[0] *= e1.x;
-          s1[1] *= e1.y;
-          s1[2] *= e1.x;
-          s1[3] *= e1.y;
+          {
+            // the decay as packed multiplies on the accumulator pairs
+            const f32x2 ev0 = f2(e0.x, e0.y), ev1 = f2(e1.x, e1.y);
+            f32x2 p0 = mul2(f2(s0[0], s0[1]), ev0), p1 = mul2(f2(s0[2], s0[3]), ev0);
+            f32x2 p2 = mul2(f2(s1[0], s1[1]), ev1), p3 = mul2(f2(s1[2], s1[3]), ev1);
+            s0[0] = f2lo(p0);
+            s0[1] = f2hi(p0);
+            s0[2] = f2lo(p1);
+            s0[3] = f2hi(p1);
+            s1[0] = f2lo(p2);
+            s1[1] = f2hi(p2);
+            s1[2] = f2lo(p3);
+            s1[3] = f2hi(p3);
+          }
           mma16816(accU[m][0], a, bw[0], bw[1]);
           mma16816(accU[m][1], a, bw[2], bw[3]);
           mma16816(accO[m][0], a, bq[0], bq[1]);
