@@ -218,9 +218,13 @@ KDA_API size_t kda_chunk_fwd_workspace_size(int B, int H, int T, int dk, int dv)
  * start and Phi (dk x dk) the end state with v = 0 from the identity; each
  * chain is cut into `segments` pieces of whole 32-token units, the pieces'
  * (Phi, S_loc) are computed in parallel, chained in fp32, and every piece is
- * then run from its start state.  Work grows by about (2P - 3) / P for P
- * segments and runs on otherwise idle SMs.  Results equal the unsegmented
- * call up to rounding order.
+ * then run from its start state.  The pieces are of equal length, or the
+ * first is twice as long as the others when a model of the two launches on
+ * the device's SMs says that finishes first (the first piece then runs beside
+ * two rounds of the others' (Phi, S_loc) work).  Work grows by about
+ * (2P - 3) / P for P segments and runs on otherwise idle SMs.  Results equal
+ * the unsegmented call up to rounding order; the workspace size does not
+ * depend on the split.
  * Requires bf16 inputs, dk = dv = 128 and a fixed-length batch (cu_seqlens
  * NULL; else KDA_ERR_UNSUPPORTED_SHAPE / KDA_ERR_INVALID_ARG) with B * T
  * below 2^31.  args->path picks the kernel that runs the pieces:
