@@ -247,9 +247,10 @@ KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* args, int segments, void
  * the recurrence of "Kimi K3 Deep Dive", section "Core Innovation 1"), in fp32
  * on CUDA cores, in chunked (WY) form: a forward pass that stores the state at
  * every 16-token chunk start and a reverse pass that carries the state
- * gradient and stores it at every chunk end (one kernel launch, run side by
- * side), then one parallel pass over all chunks for the remaining gradients
- * (a second launch on `stream`).
+ * gradient and stores it at every chunk end, then one item per chunk for the
+ * remaining gradients, all in one persistent kernel launch on `stream` whose
+ * CTAs take the recurrences first and then the chunk items of the chains
+ * whose recurrences are done.
  * Requires dk = dv = 128 and a fixed-length batch.  Layouts as kda_chunk_fwd:
  * q, k, theta, dq, dk, dtheta [B,T,H,dk]; v, d_out, dv [B,T,H,dv]; beta,
  * dbeta [B,T,H]; init_state, d_final, d_init [B,H,dk,dv] fp32 (each of the
@@ -262,8 +263,8 @@ KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* args, int segments, void
  * per (sequence, head) chain rounded up to 256 bytes), 16-byte aligned,
  * caller-owned, scratch until the stream has passed the call; it needs no
  * initial contents (the call clears the queue with a memset on `stream`
- * before its one kernel launch).  The library
- * allocates nothing.  A given log-decay (KDA_GATE_LOG_DECAY) has the forward
+ * before its kernel launch).  The library allocates nothing.  A given
+ * log-decay (KDA_GATE_LOG_DECAY) has the forward
  * pass's limit: the in-chunk sum of |g| below about 88.  Returns KDA_OK or
  * KDA_ERR_*.
  */
