@@ -238,6 +238,12 @@ KDA_API size_t kda_chunk_fwd_workspace_size(int B, int H, int T, int dk, int dv)
  * nothing.  Returns KDA_OK or KDA_ERR_*.
  */
 KDA_API size_t kda_segmented_workspace_size(int B, int H, int T, int dk, int dv, int segments);
+/* Test hook (host only, no counterpart on the pages): the plan of a
+ * segmented call on a device with `sms` SMs (0: equal pieces) -- out[0] the
+ * number of segments, out[1] the tokens of segment 0, out[2] the tokens of
+ * each later segment (the last may be shorter).  KDA_OK or
+ * KDA_ERR_INVALID_ARG. */
+KDA_API int kda_debug_segment_plan(int B, int H, int T, int segments, int sms, int64_t* out);
 KDA_API int kda_chunk_fwd_segmented(const kda_fwd_args* args, int segments, void* workspace,
                                     size_t workspace_bytes, cudaStream_t stream);
 

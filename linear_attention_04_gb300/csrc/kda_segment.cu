@@ -239,3 +239,16 @@ int launch_segmented(const FwdParams& p, int segments, void* ws, size_t ws_bytes
 }
 
 }  // namespace kda
+
+// Test hook: the segment plan of a call on a device with `sms` SMs (0: equal
+// segments), as out[0] = segments, out[1] = tokens of segment 0, out[2] =
+// tokens of each later segment (the last may be shorter).
+extern "C" KDA_API int kda_debug_segment_plan(int B, int H, int T, int segments, int sms,
+                                              int64_t* out) {
+  if (!out || B <= 0 || H <= 0 || T < 0 || sms < 0) return KDA_ERR_INVALID_ARG;
+  const kda::SegPlan pl = kda::plan(B, H, T, segments, sms);
+  out[0] = pl.P;
+  out[1] = pl.L0tok;
+  out[2] = pl.Ltok;
+  return KDA_OK;
+}

@@ -290,3 +290,56 @@ def test_binding_rejects_a_mismatched_out_before_the_c_call():
                                                 torch.zeros(1, 32, 2, 128), torch.zeros(1, 2, 64, 128))
     with pytest.raises(ValueError, match="theta"):
         binding.kda_chunk_fwd(q, k, v, th[:, :16].contiguous(), be)
+
+
+def _list_schedule(jobs, sms):
+    import heapq
+    free = [0] * sms
+    end = 0
+    for j in jobs:
+        t = heapq.heappop(free) + j
+        heapq.heappush(free, t)
+        end = max(end, t)
+    return end
+
+
+def _model(chains, P, n, u0, u, sms):
+    # launch 1: segment 0 of every chain, then two jobs per segment 1 .. P-2;
+    # launch 2: one job per segment 1 .. P-1 (the last what is left)
+    j1 = [u0] * chains + [u] * (chains * 2 * (P - 2))
+    j2 = []
+    for s in range(1, P):
+        j2 += [u if s < P - 1 else n - u0 - (P - 2) * u] * chains
+    return _list_schedule(j1, sms) + _list_schedule(j2, sms)
+
+
+@pytest.mark.parametrize("B,H,T,P,sms", [(1, 32, 262144, 5, 152), (1, 32, 262144, 4, 152),
+                                         (1, 32, 262144, 6, 152), (2, 3, 3000, 3, 152),
+                                         (1, 32, 2048, 5, 152), (1, 32, 262144, 5, 0)])
+def test_segment_plan_host_logic(B, H, T, P, sms):
+    # the planner keeps equal segments unless a first segment of twice the
+    # others' length finishes first under a list-scheduling model of the two
+    # launches (restated here on its own)
+    lib = binding.load()
+    lib.kda_debug_segment_plan.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int64)]
+    out = (ctypes.c_int64 * 3)()
+    assert lib.kda_debug_segment_plan(B, H, T, P, sms, out) == 0
+    nseg, l0, l = out[0], out[1], out[2]
+    n = -(-T // 32)                      # 32-token units
+    per = -(-n // P)
+    assert nseg == -(-n // per)
+    equal = (per * 32, per * 32)
+    u = (n + P) // (P + 1)
+    doubled = (2 * u * 32, u * 32)
+    chains = B * H
+    pick = equal
+    if sms > 0 and nseg >= 3 and 2 * u + (nseg - 2) * u < n and \
+            _model(chains, nseg, n, 2 * u, u, sms) < _model(chains, nseg, n, per, per, sms):
+        pick = doubled
+    assert (l0, l) == pick
+    # the segments cover the sequence
+    assert l0 + (nseg - 1) * l >= T > l0 + (nseg - 2) * l
+    if (B, H, T, P, sms) == (1, 32, 262144, 5, 152):
+        assert (l0, l) == doubled      # the long workload's plan
+    if sms == 0 or chains < 8:
+        assert (l0, l) == equal
